@@ -1,0 +1,418 @@
+"""SSD forward-scan benchmark: tokens/s on GB300 through the library's C ABI.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one pass of the whole forward scan (chunk_cumsum, chunk_state, state_passing,
+chunk_scan) over one batch of seeded synthetic input already resident in HBM.  L2 is
+flushed (a 256 MiB write, outside the timed events) before every timed step.  Kernel times
+come from CUDA events recorded on the launch stream between the four step launches.
+``--impl reference`` times the float64 CPU oracle instead, on a bounded sample of the same
+workload.  Rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "mamba2_130m_layer"
+METRIC = "SSD forward tokens/s on 1 GB300 + per-kernel % of HBM/tensor roofline"
+KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="approximate CPU time budget of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- accounting
+
+
+def algorithmic(shape):
+    """Minimum HBM bytes and useful FLOPs per launch of each kernel (the roofline inputs)."""
+    b, L, H, P, N, G, Q = (shape[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
+                                               "ngroups", "chunk"))
+    e = 2 if shape["io_dtype"] == "bf16" else 4
+    nc = -(-L // Q)
+    st = b * nc * H * P * N                      # elements of S / hprev
+    cs = b * H * nc * Q * 4                      # bytes of one cs2 / dtT array
+    by = {
+        "chunk_cumsum": b * L * H * 4 + H * 4 + 2 * cs,
+        "chunk_state": b * L * H * P * e + b * L * G * N * e + 2 * cs + st * 4,
+        "state_passing": st * 4 + b * H * nc * 4 + st * e + 2 * b * H * P * N * 4,
+        "chunk_scan": 2 * b * L * H * P * e + 2 * b * L * G * N * e + 2 * cs + st * e + H * 4,
+    }
+    fl = {
+        "chunk_cumsum": 2 * b * L * H,
+        "chunk_state": 2 * b * nc * H * Q * P * N,
+        "state_passing": 2 * st,
+        "chunk_scan": (2 * b * nc * G * (Q * (Q + 1) // 2) * N + 2 * b * nc * H * (Q * (Q + 1) // 2) * P
+                       + 2 * b * nc * H * Q * P * N),
+    }
+    if shape["init"]:
+        by["state_passing"] += b * H * P * N * 4
+    return by, fl
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm=float(pk["hbm_gbs"]), bf16=float(pk["bf16_tflops"]),
+                    bf16_sus=float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def source_digest(kernel):
+    files = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state_tc.cu",
+             "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu"}
+    p = os.path.join(ROOT, "state_space_model_02_gb300", "csrc", files[kernel])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if its kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "%s__%s.txt" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"^dram_bytes_per_launch\s*=\s*([0-9.eE+]+)", text, re.M)
+    h = re.search(r"^source_sha256_16\s*=\s*([0-9a-f]+)", text, re.M)
+    if not m or not h or h.group(1) != source_digest(kernel):
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- CPU baseline
+
+
+def cpu_baseline(inp, budget_s):
+    """The float64 oracle as it stands, on the host cores, over a bounded sample of the
+    workload: whole (batch, head) sequences, as many as fit the time budget."""
+    from oracle import ref
+
+    b, L, H, P = inp.x.shape
+    pairs = [(bb, hh) for bb in range(b) for hh in range(H)]
+    threads = ref.num_threads()
+    # probe one pair per thread, then size the sample to the budget
+    probe = pairs[:max(1, min(len(pairs), threads))]
+    t0 = time.perf_counter()
+    ref.recurrence(inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.init, chunk=inp.chunk,
+                   pairs=np.array(probe), want_final=True)
+    dt_probe = time.perf_counter() - t0
+    per_pair = dt_probe / len(probe)
+    n = int(min(len(pairs), max(len(probe), budget_s / max(per_pair, 1e-9))))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    n = min(n, len(pairs))
+    sample = pairs[:n]
+    reps, el = 0, 0.0
+    while reps == 0 or (el < budget_s and reps < 100):   # repeat small workloads up to the budget
+        t0 = time.perf_counter()
+        ref.recurrence(inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.init, chunk=inp.chunk,
+                       pairs=np.array(sample), want_final=True)
+        el += time.perf_counter() - t0
+        reps += 1
+    tokens = reps * b * L * (len(sample) / (b * H))  # whole-layer tokens the sample amounts to
+    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d (batch, head) sequences of %d tokens x %d passes, float64 "
+                      "recurrence, %.1f s" % (len(sample), b * H, L, reps, el)}
+
+
+# ------------------------------------------------------------------------------ arms
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from state_space_model_02_gb300 import synth
+
+    inp = synth.make_config(args.workload, seed=args.seed)
+    shape = dict(synth.CONFIGS[args.workload])
+    vals = []
+    per = max(1.0, args.cpu_seconds / max(1, args.steps))
+    base = None
+    for _ in range(args.steps):
+        base = cpu_baseline(inp, per)
+        vals.append(base["value"])
+    v = float(np.median(vals))
+    tokens = shape["batch"] * shape["seqlen"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tokens / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, **shape},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": base["cores"], "kind": "oracle",
+                             "sample": base["sample"]},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from state_space_model_02_gb300 import build as cuda_build
+    from state_space_model_02_gb300 import ssd, synth
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cuda_build.build()
+    ssd.load_library()
+
+    shape = dict(synth.CONFIGS[args.workload])
+    inp = synth.make_config(args.workload, seed=args.seed)
+    bf16 = inp.io_dtype == "bf16"
+
+    def io(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else np.ascontiguousarray(a))
+        return t.view(torch.bfloat16) if bf16 else t
+
+    host = dict(x=io(inp.x), dt=torch.from_numpy(inp.dt), A=torch.from_numpy(inp.A), B=io(inp.B),
+                C=io(inp.C), D=torch.from_numpy(inp.D),
+                init=None if inp.init is None else torch.from_numpy(inp.init))
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    prob = ssd.problem_of(d["x"], d["B"], inp.chunk)
+    wsbuf = ssd.alloc_workspace(prob, dev)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((prob.batch, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        ssd.chunk_cumsum(prob, d["dt"], d["A"], wsbuf, stream)
+        if evs:
+            evs[1].record(stream)
+        ssd.chunk_state(prob, d["x"], d["B"], wsbuf, stream)
+        if evs:
+            evs[2].record(stream)
+        ssd.state_passing(prob, d["init"], fin, wsbuf, stream)
+        if evs:
+            evs[3].record(stream)
+        ssd.chunk_scan(prob, d["x"], d["B"], d["C"], d["D"], y, wsbuf, stream)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    status = ssd.read_status(wsbuf, stream)
+    if status != 0:
+        raise RuntimeError("kernel status %d during warm-up" % status)
+
+    clocks = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)         # evict L2: untimed, outside the step's events
+        step(evs[k])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    per_kernel = {n: [] for n in KERNELS}
+    totals = []
+    for e in evs:
+        for i, n in enumerate(KERNELS):
+            per_kernel[n].append(e[i].elapsed_time(e[i + 1]))
+        totals.append(e[0].elapsed_time(e[4]))
+    ms_step = float(np.sum(totals) / args.steps)
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = prob.batch * prob.seqlen
+    value = ws * tokens / (ms_step * 1e-3)
+
+    # roofline of every kernel; the dominant (largest share) is reported
+    by, fl = algorithmic(shape)
+    peaks = load_peaks()
+    kern = {}
+    for n in KERNELS:
+        ms = float(np.mean(per_kernel[n]))
+        t_hbm = by[n] / (peaks["hbm"] * 1e9)
+        t_ten = fl[n] / (peaks["bf16"] * 1e12) if n in ("chunk_state", "chunk_scan") else 0.0
+        bound = "hbm" if t_hbm >= t_ten else "tensor"
+        ach = by[n] / (ms * 1e-3) / 1e9 if bound == "hbm" else fl[n] / (ms * 1e-3) / 1e12
+        peak = peaks["hbm"] if bound == "hbm" else peaks["bf16"]
+        kern[n] = {"us": 1e3 * ms, "share": ms / ms_step, "bound": bound, "achieved": ach, "peak": peak,
+                   "frac": ach / peak, "alg_bytes": by[n], "alg_flops": fl[n],
+                   "tensor_frac_of_peak": fl[n] / (ms * 1e-3) / 1e12 / peaks["bf16"]}
+    dom = max(KERNELS, key=lambda n: kern[n]["us"])
+    kd = kern[dom]
+    tr = profiled_traffic(dom, args.workload)
+    roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"], "peak": kd["peak"],
+                "unit": "GB/s" if kd["bound"] == "hbm" else "TFLOP/s", "frac": kd["frac"],
+                "traffic": tr, "peak_source": peaks["src"] + " (MEASURED_PEAKS.json burst)"
+                if peaks["src"] == "measured" else "fallback"}
+
+    # end to end through the public API: pinned host in, result back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        f_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+        d2h = y_host.numel() * y_host.element_size() + f_host.numel() * f_host.element_size()
+        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in pin.items()}
+
+        def e2e_step():
+            for k, v in pin.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            yy, ff = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
+                             chunk=inp.chunk, init_state=dev_in["init"], y=y, final_state=fin, workspace=wsbuf)
+            y_host.copy_(yy, non_blocking=True)
+            f_host.copy_(ff, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+    plan = ssd.kernel_plan(prob)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": args.workload, **shape,
+                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "tensor_core_steps": {"chunk_state": bool(plan & 1), "chunk_scan": bool(plan & 2)}},
+        "roofline": roofline,
+        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in kern[n].items()}
+                    for n in KERNELS},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": len(KERNELS) * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

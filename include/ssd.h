@@ -1,0 +1,167 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked forward scan.
+ *
+ * The layer (per head h, with B/C group g = h / (H / G)):
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * outer(x_t, B_t)      (P x N state)
+ *     y_t = h_t @ C_t + D_h * x_t
+ * computed chunk-wise in the four steps that "Mamba-2 cuda-tile forward pass
+ * kernels" (devotd.net) section 2 describes: an in-chunk log2-domain cumsum
+ * of A*dt (chunk_cumsum, with its listing), the states at every chunk start
+ * and after the last chunk (fwd_pass_state, here split into chunk_state and
+ * state_passing), and the token outputs from the chunk-start states with the
+ * intermediate C.B^T tile kept on chip (compute_out, here chunk_scan).
+ *
+ * Conventions for every entry point
+ *   - All tensors are dense, row-major, contiguous, in DEVICE memory:
+ *       x, y        (batch, seqlen, nheads, headdim)     io dtype
+ *       dt          (batch, seqlen, nheads)              float32, the final step size
+ *       A, D        (nheads)                             float32
+ *       B, C        (batch, seqlen, ngroups, dstate)     io dtype
+ *       init_state, final_state (batch, nheads, headdim, dstate)  float32
+ *     io dtype is float32 or bfloat16 (ssd_shape.io_dtype).
+ *   - Device pointers must be 16-byte aligned (SSD_ERR_ALIGN otherwise).
+ *   - The caller owns every buffer, the workspace included.  The library
+ *     allocates no device memory, keeps no per-call state, and never
+ *     modifies its inputs.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Outputs are valid once the
+ *     stream has been synchronised.  No call synchronises the stream except
+ *     ssd_read_status().
+ *   - Errors are returned as ssd_status; nothing aborts or throws across the
+ *     ABI.  Argument checks happen on the host before any launch; a failed
+ *     check launches nothing.  ssd_last_error() gives a one-line detail of the
+ *     last failure on the calling thread.
+ *   - Kernels that wait on on-chip barriers give every wait a time limit; on
+ *     expiry they record SSD_ERR_TIMEOUT in the workspace status word, drain
+ *     their own copies, release tensor memory and return.  ssd_read_status()
+ *     reports it.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID = 1,     /* bad shape, null required pointer, bad dtype        */
+  SSD_ERR_UNSUPPORTED = 2, /* valid shape that no kernel here handles            */
+  SSD_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned            */
+  SSD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed               */
+  SSD_ERR_TIMEOUT = 5,     /* a kernel's bounded on-chip wait expired            */
+  SSD_ERR_WORKSPACE = 6    /* workspace missing or smaller than required         */
+} ssd_status;
+
+/* Kernel-selection flags (ssd_shape.flags). */
+#define SSD_FLAG_FORCE_SIMT 1u /* use the CUDA-core kernels even where the tensor-core ones apply */
+
+typedef struct {
+  int64_t batch;   /* b  >= 1                                               */
+  int64_t seqlen;  /* L  >= 1 (any length; the last chunk may be ragged)    */
+  int64_t nheads;  /* H  >= 1, a multiple of ngroups                        */
+  int64_t headdim; /* P  >= 1                                               */
+  int64_t dstate;  /* N  >= 1                                               */
+  int64_t ngroups; /* G  >= 1                                               */
+  int64_t chunk;   /* Q  in {64, 128, 256}                                  */
+  int32_t io_dtype;/* ssd_dtype of x, B, C, y                               */
+  uint32_t flags;  /* SSD_FLAG_* ; 0 for the default kernel choice          */
+} ssd_shape;
+
+/* Byte offsets of the intermediates inside a workspace (for inspection).
+ *   cs2   float32 (b, H, nc, Q): log2(e) * in-chunk inclusive cumsum of A*dt,
+ *         zero-padded past seqlen (chunk_cumsum output)
+ *   dtT   float32 (b, H, nc, Q): dt laid out per head and chunk, zero-padded
+ *   S     float32 (b, nc, H, P, N): per-chunk end state started from zero
+ *   hprev (b, nc, H, P, N): state entering each chunk; bfloat16 when
+ *         io_dtype is SSD_BF16, float32 when SSD_F32
+ *   status uint32 at offset 0: 0, or an ssd_status recorded by a kernel      */
+typedef struct {
+  size_t status, cs2, dtT, S, hprev, total;
+  int64_t nchunks;
+} ssd_workspace_layout;
+
+/* Workspace bytes ssd_fwd needs for `shape`; 0 when the shape is invalid. */
+size_t ssd_workspace_bytes(const ssd_shape* shape);
+
+/* Fills *out for `shape`.  SSD_ERR_INVALID on a bad shape or null out. */
+ssd_status ssd_get_workspace_layout(const ssd_shape* shape, ssd_workspace_layout* out);
+
+/*
+ * Full forward pass: chunk_cumsum -> chunk_state -> state_passing -> chunk_scan.
+ *   D           nullable: treated as zeros
+ *   init_state  nullable: the scan starts from the zero state
+ *   final_state nullable: not written
+ *   workspace   device buffer of >= ssd_workspace_bytes(shape) bytes,
+ *               256-byte aligned; its contents on entry are ignored and on
+ *               return hold the intermediates (see ssd_workspace_layout)
+ * y receives the outputs in io dtype (bfloat16 rounded to nearest even).
+ */
+ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                   const void* B, const void* C, const float* D, const float* init_state,
+                   void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* The four steps of ssd_fwd, one launch each, for callers that time or
+ * inspect them.  They communicate through the workspace and must run in
+ * this order on one stream. */
+
+/* Step 1, chunk_cumsum ("Mamba-2 cuda-tile forward pass kernels" section 2,
+ * first kernel and its listing): writes cs2 and dtT. */
+ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 2, chunk_state (same page, section 2, first half of fwd_pass_state):
+ * S[b,c,h] = sum_t exp2(cs2_last - cs2_t) * dt_t * outer(x_t, B_t) over the
+ * chunk's tokens.  Reads cs2/dtT, writes S. */
+ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* B,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 3, state_passing (same page, section 2, second half of fwd_pass_state:
+ * chunk order kept, independent state elements in parallel):
+ * hprev[c] = h_{c-1}, h_c = exp2(cs2_last,c) * h_{c-1} + S_c, h_{-1} = init.
+ * Reads S and cs2, writes hprev and (if non-null) final_state. */
+ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state,
+                             float* final_state, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Step 4, chunk_scan (same page, section 2, compute_out):
+ * y_i = sum_{j<=i in chunk} exp2(cs2_i - cs2_j) dt_j (C_i.B_j) x_j
+ *       + exp2(cs2_i) C_i . hprev + D x_i.   Reads cs2/dtT/hprev, writes y. */
+ssd_status ssd_chunk_scan(const ssd_shape* shape, const void* x, const void* B, const void* C,
+                          const float* D, void* y, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Synchronises `stream`, then reads the workspace status word: SSD_OK, or
+ * the status a kernel recorded (SSD_ERR_TIMEOUT).  SSD_ERR_CUDA if the
+ * synchronisation or the read fails. */
+ssd_status ssd_read_status(const void* workspace, void* stream);
+
+/* Diagnostic: launches one block that waits, with the library's bounded
+ * wait, on an on-chip barrier that nothing ever completes, limited to
+ * `timeout_ns`, and records SSD_ERR_TIMEOUT in the status word at
+ * `status_word` (a device uint32).  Exercises the timeout path without any
+ * fault.  0 < timeout_ns <= 1e9. */
+ssd_status ssd_selftest_wait_timeout(uint32_t* status_word, uint64_t timeout_ns, void* stream);
+
+/* Static description of a status code. */
+const char* ssd_status_str(ssd_status status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* ssd_last_error(void);
+
+/* Which kernel family ssd_fwd would use for each step of `shape`:
+ * bit 0 chunk_state on tensor cores, bit 1 chunk_scan on tensor cores.
+ * -1 for an invalid shape. */
+int ssd_kernel_plan(const ssd_shape* shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

@@ -1,0 +1,304 @@
+// chunk_state on the 5th-generation tensor cores (tcgen05) -- step 2 of the SSD forward scan.
+//
+// "Mamba-2 cuda-tile forward pass kernels" (devotd.net), section 1: each chunk's work is
+// turned into matrix products for the Tensor Cores; section 2 (fwd_pass_state): the state a
+// chunk contributes, before chaining across chunks, is
+//     S[b,c,h][p,n] = sum_t x~[t,(h,p)] * B[t,n],   x~[t,(h,p)] = 2^{cs2_last - cs2_t} dt_t x[t,h,p]
+// a contraction over the chunk's Q tokens.  Section 3 swaps MMA operands to suit the 5th-gen
+// Tensor Core operand layout; here two heads are stacked on the MMA M axis (M = 2 x P = 128,
+// x is (token, head, p) so two neighbouring heads are one contiguous 128-wide row) and the
+// state dimension is the N axis, so both operands come straight from TMA in MN-major
+// 128-byte-swizzled form with no transposition.
+//
+// One CTA = (head pair, n-tile, chunk, batch), 128 threads, no warp specialisation:
+//   thread 0 issues TMA loads (2-stage ring over 64-token k-blocks) and the MMAs;
+//   all threads scale the x tile in shared memory by the per-token decay weight
+//   (one scale per 128-byte row, so the swizzle is irrelevant), then drain the f32
+//   accumulator from tensor memory and stage it for TMA stores of S.
+// Requirements (checked by chunk_state_tc_ok): bf16 I/O, P = 64, Q in {128, 256},
+// N in {64, 128, 256, 512} (512 runs as two 256-wide n-tiles).
+#include "ptx.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kBox = 8192;  // one TMA box: 64 rows x 128 bytes
+
+struct CsParams {
+  int32_t L, H, nc, Q, N, hpg, pairs_per_group, n_tiles;
+  const float* cs2;
+  const float* dtT;
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+template <int NT>
+struct CsSmem {
+  static constexpr uint32_t kX = 2 * kBox;            // x: two heads x (64 tokens x 64 p)
+  static constexpr uint32_t kB = (NT / 64) * kBox;    // B: NT/64 boxes of (64 tokens x 64 n)
+  static constexpr uint32_t kStage = kX + kB;
+  static constexpr uint32_t kTiles = 2 * kStage;      // 2-stage ring; reused as epilogue staging
+  static constexpr uint32_t kW = kTiles;              // float w[2][256]
+  static constexpr uint32_t kBars = kW + 2 * 256 * 4; // full[2], empty[2], done, drain
+  static constexpr uint32_t kTmemSlot = kBars + 6 * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kUsed = kAbort + 4;
+  static constexpr uint32_t kAlloc = kUsed + 1024;    // slack for 1024-byte alignment
+  static constexpr uint32_t kEpiCols = NT < 128 ? NT : 128;
+  static_assert(4 * 2 * kBox <= kTiles || NT == 64, "epilogue staging must fit in the ring");
+};
+
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
+  return pack_bf16x2(bf16lo_to_f32(v) * w, bf16hi_to_f32(v) * w);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_B,
+                          const __grid_constant__ CUtensorMap tm_S, const CsParams prm) {
+  using SM = CsSmem<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  const int nt = blockIdx.x % prm.n_tiles;
+  const int pair = blockIdx.x / prm.n_tiles;
+  const int g = pair / prm.pairs_per_group;
+  const int h0 = g * prm.hpg + 2 * (pair % prm.pairs_per_group);
+  const int nh = min(2, (g + 1) * prm.hpg - h0);  // 1 when the group has an odd head count
+  const int c = blockIdx.y, b = blockIdx.z;
+  const int Q = prm.Q, kblocks = Q / 64;
+
+  float* wsm = reinterpret_cast<float*>(smem + SM::kW);
+  const uint32_t bar_full = sb + SM::kBars, bar_empty = bar_full + 16, bar_done = bar_full + 32,
+                 bar_drain = bar_full + 40;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM::kAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlot);
+
+  if (tid == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_B);
+    prefetch_tmap(&tm_S);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), NT);
+    tmem_relinquish();
+  }
+  // decay weights of the (up to) two heads: w[k][t] = 2^(cs2_last - cs2_t) * dt_t
+  for (int e = tid; e < 2 * Q; e += kThreads) {
+    const int k = e / Q, t = e % Q;
+    float w = 0.f;
+    if (k < nh) {
+      const int64_t row = ((int64_t(b) * prm.H + h0 + k) * prm.nc + c) * Q;
+      w = ex2(prm.cs2[row + Q - 1] - prm.cs2[row + t]) * prm.dtT[row + t];
+    }
+    wsm[k * 256 + t] = w;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, NT, 1, 1);
+
+  // thread-0 bookkeeping of loads in flight (for the drain on abort)
+  int issued = 0, consumed = 0;
+  auto issue = [&](int kb) {
+    const int s = kb & 1;
+    const uint32_t st = sb + s * SM::kStage;
+    const uint32_t full = bar_full + 8 * s;
+    const int t0 = c * Q + kb * 64;
+    mbar_arrive_expect_tx(full, SM::kStage);
+    tma_load_3d(st, &tm_x, full, h0 * 64, t0, b);
+    tma_load_3d(st + kBox, &tm_x, full, (h0 + 1) * 64, t0, b);
+#pragma unroll
+    for (int j = 0; j < NT / 64; ++j)
+      tma_load_3d(st + SM::kX + j * kBox, &tm_B, full, g * prm.N + nt * NT + j * 64, t0, b);
+    issued = kb + 1;
+  };
+
+  if (tid == 0) {
+    issue(0);
+    if (kblocks > 1) issue(1);
+  }
+  for (int kb = 0; kb < kblocks; ++kb) {
+    const int s = kb & 1;
+    const uint32_t ph = (kb >> 1) & 1;
+    const bool ok = mbar_wait(bar_full + 8 * s, ph, ctl);
+    if (tid == 0 && ok) consumed = kb + 1;
+    if (ok) {
+      // x~ = w * x in place: 1024 16-byte chunks (two boxes x 64 rows x 8), 8 per thread
+      uint8_t* xs = smem + s * SM::kStage;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = tid + kThreads * i;
+        const int k = q >> 9, r = (q >> 3) & 63;
+        const float w = wsm[k * 256 + kb * 64 + r];
+        uint4* p = reinterpret_cast<uint4*>(xs + q * 16);
+        uint4 v = *p;
+        v.x = scale_bf16x2(v.x, w);
+        v.y = scale_bf16x2(v.y, w);
+        v.z = scale_bf16x2(v.z, w);
+        v.w = scale_bf16x2(v.w, w);
+        *p = v;
+      }
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (tid == 0 && !*abort_flag) {
+      tc_fence_after();
+      const uint32_t xa = sb + s * SM::kStage, ba = xa + SM::kX;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_f16(tmem, sdesc_sw128(xa + k * 2048, kBox, 1024), sdesc_sw128(ba + k * 2048, kBox, 1024),
+                 kIdesc, (kb | k) != 0 ? 1u : 0u);
+      umma_commit(bar_empty + 8 * s);
+      if (kb + 2 < kblocks) {
+        // reuse stage s once the MMAs just issued have read it
+        if (mbar_wait(bar_empty + 8 * s, ph, ctl)) issue(kb + 2);
+      }
+    }
+  }
+
+  // all MMAs complete -> accumulator readable
+  if (tid == 0) umma_commit(bar_done);
+  // uniform across the CTA: the epilogue below contains block-wide barriers
+  const bool acc_ok = __syncthreads_and(mbar_wait(bar_done, 0, ctl) && !*abort_flag) != 0;
+  tc_fence_after();
+
+  if (acc_ok) {
+    constexpr int kEpi = SM::kEpiCols;
+    for (int half = 0; half < NT / kEpi; ++half) {
+      if (half > 0) {
+        if (tid == 0) bulk_wait_read0();
+        __syncthreads();
+      }
+      const int k = tid >> 6, r = tid & 63;
+#pragma unroll 1
+      for (int q = 0; q < kEpi / 32; ++q) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + half * kEpi + q * 32, v);
+        tmem_ld_wait();
+        uint8_t* box = smem + (q * 2 + k) * kBox;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(box + r * 128 + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        for (int q = 0; q < kEpi / 32; ++q)
+          for (int kk = 0; kk < nh; ++kk)
+            tma_store_2d(&tm_S, sb + (q * 2 + kk) * kBox, nt * NT + half * kEpi + q * 32,
+                         ((b * prm.nc + c) * prm.H + h0 + kk) * 64);
+        bulk_commit();
+      }
+    }
+  }
+
+  // teardown: drain whatever is still in flight, then release tensor memory
+  if (tid == 0) {
+    for (int kb = consumed; kb < issued; ++kb)
+      (void)mbar_drain(bar_full + 8 * (kb & 1), (kb >> 1) & 1, kWaitLimitNs);
+    if (!acc_ok) {
+      umma_commit(bar_drain);
+      (void)mbar_drain(bar_drain, 0, kWaitLimitNs);
+    }
+    bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, NT);
+  }
+}
+
+template <int NT>
+cudaError_t launch_nt(const Problem& p, const CUtensorMap& tx, const CUtensorMap& tb,
+                      const CUtensorMap& ts, const CsParams& prm, cudaStream_t st) {
+  using SM = CsSmem<NT>;
+  auto kern = chunk_state_tc_kernel<NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.G * prm.pairs_per_group * prm.n_tiles),
+                  static_cast<unsigned>(p.nc), static_cast<unsigned>(p.b));
+  kern<<<grid, kThreads, SM::kAlloc, st>>>(tx, tb, ts, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_state_tc_ok(const Problem& p) {
+  return p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) &&
+         (p.N == 64 || p.N == 128 || p.N == 256 || p.N == 512) &&
+         p.L <= (int64_t(1) << 31) - 1 && p.b * p.nc * p.H * p.P < (int64_t(1) << 31);
+}
+
+cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
+                                  const float* dtT, float* S, uint32_t* status, cudaStream_t st,
+                                  const char** why) {
+  const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
+  CUtensorMap tx, tb, ts;
+  {
+    const uint64_t dims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
+    const uint64_t strides[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
+    const uint32_t box[3] = {64, 64, 1};
+    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
+    const uint64_t strides[2] = {uint64_t(p.G * p.N * 2), uint64_t(p.L * p.G * p.N * 2)};
+    const uint32_t box[3] = {64, 64, 1};
+    if (!encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {uint64_t(p.N), uint64_t(p.b * p.nc * p.H * p.P)};
+    const uint64_t strides[1] = {uint64_t(p.N * 4)};
+    const uint32_t box[2] = {32, 64};
+    if (!encode_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  }
+  CsParams prm;
+  prm.L = static_cast<int32_t>(p.L);
+  prm.H = static_cast<int32_t>(p.H);
+  prm.nc = static_cast<int32_t>(p.nc);
+  prm.Q = static_cast<int32_t>(p.Q);
+  prm.N = static_cast<int32_t>(p.N);
+  prm.hpg = static_cast<int32_t>(p.hpg);
+  prm.pairs_per_group = static_cast<int32_t>((p.hpg + 1) / 2);
+  prm.n_tiles = static_cast<int32_t>(p.N / NT);
+  prm.cs2 = cs2;
+  prm.dtT = dtT;
+  prm.status = status;
+  prm.wait_ns = kWaitLimitNs;
+  switch (NT) {
+    case 64: return launch_nt<64>(p, tx, tb, ts, prm, st);
+    case 128: return launch_nt<128>(p, tx, tb, ts, prm, st);
+    case 256: return launch_nt<256>(p, tx, tb, ts, prm, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ssd

@@ -1,0 +1,82 @@
+// ssd_internal.h -- problem description, workspace layout and kernel launchers shared by the
+// translation units of libssd.so.  Host-side only declarations; no torch types anywhere.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// One problem, with every size the kernels need precomputed on the host.
+struct Problem {
+  int64_t b, L, H, P, N, G, Q;
+  int64_t nc;      // number of chunks, ceil(L / Q)
+  int64_t hpg;     // heads per group, H / G
+  bool io_bf16;    // x, B, C, y are bf16 (else f32); hprev has the same element type
+  uint32_t flags;  // SSD_FLAG_*
+};
+
+// Byte offsets inside the caller's workspace.  Each region is 1024-byte aligned.
+struct Layout {
+  size_t status, cs2, dtT, S, hprev, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline Layout make_layout(const Problem& p) {
+  Layout l{};
+  const size_t cs_bytes = static_cast<size_t>(p.b * p.H * p.nc * p.Q) * 4u;
+  const size_t st_elems = static_cast<size_t>(p.b * p.nc * p.H * p.P * p.N);
+  l.status = 0;
+  l.cs2 = 1024;
+  l.dtT = align_up(l.cs2 + cs_bytes, 1024);
+  l.S = align_up(l.dtT + cs_bytes, 1024);
+  l.hprev = align_up(l.S + st_elems * 4u, 1024);
+  l.total = align_up(l.hprev + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
+  return l;
+}
+
+// Default limit of one bounded on-chip wait (ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ---- launchers (each returns the launch's cudaError_t; none synchronises) ----
+
+cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
+                                float* dtT, cudaStream_t st);
+
+cudaError_t launch_state_passing(const Problem& p, const float* S, const float* cs2,
+                                 const float* init, void* hprev, float* final_state,
+                                 cudaStream_t st);
+
+cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void* B, const float* cs2,
+                                    const float* dtT, float* S, cudaStream_t st);
+
+cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
+                                   const float* D, const float* cs2, const float* dtT,
+                                   const void* hprev, void* y, cudaStream_t st);
+
+// Tensor-core (tcgen05) kernels.  Applicability is decided by the *_tc_ok predicates.
+bool chunk_state_tc_ok(const Problem& p);
+bool chunk_scan_tc_ok(const Problem& p);
+
+cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
+                                  const float* dtT, float* S, uint32_t* status, cudaStream_t st,
+                                  const char** why);
+
+cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
+                                 const float* D, const float* cs2, const float* dtT,
+                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
+                                 const char** why);
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Tensor-map encoder (driver entry point resolved once through the runtime).
+// rank 2 or 3; dims/box innermost first; strides in bytes for dims 1..rank-1.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle, const char** why);
+
+int num_sms_current_device();
+
+}  // namespace ssd

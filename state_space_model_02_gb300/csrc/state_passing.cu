@@ -1,0 +1,132 @@
+// state_passing -- step 3 of the SSD forward scan.
+//
+// "Mamba-2 cuda-tile forward pass kernels" (devotd.net), section 2: the second kernel
+// produces the hidden state at the start of every chunk and the state after the last chunk,
+// keeping chunk order while independent pieces of the state run in parallel.  Per element
+// (b, h, p, n) of the P x N state:
+//     hprev[c] = h_{c-1},   h_c = 2^{cs2_last(c)} * h_{c-1} + S_c,   h_{-1} = init (or 0),
+//     final    = h_{nc-1}
+// where cs2_last(c) is the log2-domain decay of the whole chunk (the last entry of the
+// chunk_cumsum row; zero padding past the sequence end leaves it unchanged).
+//
+// The loop over chunks is a dependent FMA chain per element, so the kernel is bound by HBM
+// latency x bandwidth: each thread owns 4 consecutive state elements (one float4 of S per
+// chunk) and keeps kDepth chunks of S in flight in registers ahead of the chain.
+#include "ptx.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kDepth = 8;
+
+__device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
+  uint2 u;
+  u.x = pack_bf16x2(v.x, v.y);
+  u.y = pack_bf16x2(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+template <typename HT>
+__global__ void __launch_bounds__(256) state_passing_vec4_kernel(
+    const float* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
+    HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
+    int64_t Q, int64_t total4) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total4) return;
+  const int64_t per_bh = PN / 4;
+  const int64_t bh = idx / per_bh, e = (idx % per_bh) * 4;
+  const int64_t bi = bh / H, h = bh % H;
+  const int64_t cstride = H * PN;  // elements between chunks in S / hprev
+  const float* Sp = S + (bi * nc * H + h) * PN + e;
+  HT* Hp = hprev + (bi * nc * H + h) * PN + e;
+  const float* dec = cs2 + bh * nc * Q + (Q - 1);
+
+  float4 hv = init ? __ldg(reinterpret_cast<const float4*>(init + bh * PN + e))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 sbuf[kDepth];
+  float dbuf[kDepth];
+#pragma unroll
+  for (int k = 0; k < kDepth; ++k) {
+    if (k < nc) {
+      sbuf[k] = __ldcs(reinterpret_cast<const float4*>(Sp + k * cstride));
+      dbuf[k] = __ldg(dec + k * Q);
+    }
+  }
+  for (int64_t c0 = 0; c0 < nc; c0 += kDepth) {
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) {
+      const int64_t c = c0 + k;
+      if (c < nc) {
+        store4(Hp + c * cstride, hv);
+        const float d = ex2(dbuf[k]);
+        hv.x = fmaf(d, hv.x, sbuf[k].x);
+        hv.y = fmaf(d, hv.y, sbuf[k].y);
+        hv.z = fmaf(d, hv.z, sbuf[k].z);
+        hv.w = fmaf(d, hv.w, sbuf[k].w);
+        if (c + kDepth < nc) {
+          sbuf[k] = __ldcs(reinterpret_cast<const float4*>(Sp + (c + kDepth) * cstride));
+          dbuf[k] = __ldg(dec + (c + kDepth) * Q);
+        }
+      }
+    }
+  }
+  if (final_state) *reinterpret_cast<float4*>(final_state + bh * PN + e) = hv;
+}
+
+__device__ __forceinline__ void store1(float* dst, float v) { *dst = v; }
+__device__ __forceinline__ void store1(uint16_t* dst, float v) {
+  *dst = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+}
+
+// Any P*N: one element per thread, no vectorisation.
+template <typename HT>
+__global__ void __launch_bounds__(256) state_passing_scalar_kernel(
+    const float* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
+    HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
+    int64_t Q, int64_t total) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int64_t bh = idx / PN, e = idx % PN;
+  const int64_t bi = bh / H, h = bh % H;
+  const int64_t cstride = H * PN;
+  const float* Sp = S + (bi * nc * H + h) * PN + e;
+  HT* Hp = hprev + (bi * nc * H + h) * PN + e;
+  const float* dec = cs2 + bh * nc * Q + (Q - 1);
+  float hv = init ? __ldg(init + bh * PN + e) : 0.f;
+  for (int64_t c = 0; c < nc; ++c) {
+    store1(Hp + c * cstride, hv);
+    hv = fmaf(ex2(__ldg(dec + c * Q)), hv, __ldg(Sp + c * cstride));
+  }
+  if (final_state) final_state[bh * PN + e] = hv;
+}
+
+}  // namespace
+
+cudaError_t launch_state_passing(const Problem& p, const float* S, const float* cs2,
+                                 const float* init, void* hprev, float* final_state,
+                                 cudaStream_t st) {
+  const int64_t PN = p.P * p.N;
+  const bool vec = (PN % 4) == 0;
+  const int64_t total = p.b * p.H * (vec ? PN / 4 : PN);
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+  if (vec) {
+    if (p.io_bf16)
+      state_passing_vec4_kernel<uint16_t><<<blocks, 256, 0, st>>>(
+          S, cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+    else
+      state_passing_vec4_kernel<float><<<blocks, 256, 0, st>>>(
+          S, cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+  } else {
+    if (p.io_bf16)
+      state_passing_scalar_kernel<uint16_t><<<blocks, 256, 0, st>>>(
+          S, cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+    else
+      state_passing_scalar_kernel<float><<<blocks, 256, 0, st>>>(
+          S, cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssd
