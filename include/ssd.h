@@ -149,6 +149,31 @@ ssd_status ssd_read_status(const void* workspace, void* stream);
  * fault.  0 < timeout_ns <= 1e9. */
 ssd_status ssd_selftest_wait_timeout(uint32_t* status_word, uint64_t timeout_ns, void* stream);
 
+/*
+ * Forward pass without a caller-supplied workspace, for callers that cannot allocate
+ * device memory (for example a plugin inside a host application that owns the whole
+ * device-memory budget, or a serving loop that must never call the allocator).  The pages
+ * this library follows have no counterpart to it.
+ *
+ * Arguments, layouts and results are those of ssd_fwd; the scratch comes from one fixed
+ * array of SSD_NOALLOC_MAX_WORKSPACE_BYTES in the library's device image, which every GPU
+ * that loads the library keeps until the process exits.  The call allocates nothing.
+ *   - Shapes whose ssd_workspace_bytes() exceeds SSD_NOALLOC_MAX_WORKSPACE_BYTES are
+ *     rejected with SSD_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress and caches it; make that first call before any
+ *     stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the previous call's
+ *     intermediates: calls whose work overlaps on the GPU (other streams, other threads)
+ *     race on it and must be ordered by the caller.
+ *   - ssd_read_status() cannot reach the array's status word; use ssd_fwd when a kernel
+ *     time-out must be observed.
+ */
+#define SSD_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
+ssd_status ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                           const void* B, const void* C, const float* D, const float* init_state,
+                           void* y, float* final_state, void* stream);
+
 /* Static description of a status code. */
 const char* ssd_status_str(ssd_status status);
 

@@ -19,7 +19,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_E
 # Every entry point of include/ssd.h, in declaration order.
 EXPORTS = ("ssd_workspace_bytes", "ssd_get_workspace_layout", "ssd_fwd", "ssd_chunk_cumsum",
            "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_read_status",
-           "ssd_selftest_wait_timeout", "ssd_status_str", "ssd_last_error", "ssd_kernel_plan")
+           "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_status_str", "ssd_last_error",
+           "ssd_kernel_plan")
 
 
 class Shape(ctypes.Structure):
@@ -62,6 +63,7 @@ def load_library(path: str = LIB_PATH):
         "ssd_chunk_scan": ([sp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_read_status": ([vp, vp], ctypes.c_int),
         "ssd_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ctypes.c_int),
+        "ssd_fwd_noalloc": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "ssd_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "ssd_last_error": ([], ctypes.c_char_p),
         "ssd_kernel_plan": ([sp], ctypes.c_int),
