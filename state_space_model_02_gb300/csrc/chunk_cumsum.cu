@@ -8,8 +8,9 @@
 // leave this kernel as (b, H, nc, Q) float32 rows, one contiguous row per (head, chunk).
 //
 // One CTA = (chunk c, batch b, tile of 8 heads); one warp per head.  The (Q x 8) dt tile is
-// staged through shared memory with coalesced loads, then each lane sums Q/32 consecutive
-// tokens and a warp-shuffle (Kogge-Stone) scan combines the lane totals.
+// staged through shared memory with all loads in flight; each warp then scans its head's Q
+// values in rounds of 32 tokens (a warp-shuffle Kogge-Stone scan per round plus a running
+// carry), so each round writes one contiguous 128-byte row of cs2 and of dtT.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -26,47 +27,49 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
                                                            float* __restrict__ dtT, int64_t L,
                                                            int64_t H, int64_t nc) {
   constexpr int R = Q / 32;                 // tokens per lane
-  constexpr int ROW = Q + Q / 32;           // padded row: index t + t/32 is bank-conflict free
+  constexpr int ROW = Q + Q / 32;           // padded row (t + t/32) for the staging writes
   __shared__ float tile[kHeadsPerCta][ROW];
   const int64_t c = blockIdx.x, b = blockIdx.y, h0 = int64_t(blockIdx.z) * kHeadsPerCta;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  for (int e = tid; e < Q * kHeadsPerCta; e += 256) {
-    const int t = e / kHeadsPerCta, k = e % kHeadsPerCta;
+  // all loads of the tile are issued before any is consumed (Q/32 per thread in flight)
+  constexpr int kPer = Q * kHeadsPerCta / 256;
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid + 256 * i, t = e / kHeadsPerCta, k = e % kHeadsPerCta;
     const int64_t tok = c * Q + t, h = h0 + k;
-    float v = 0.f;  // zero padding past the sequence end and past the last head
-    if (tok < L && h < H) v = __ldg(dt + (b * L + tok) * H + h);
-    tile[k][t + t / 32] = v;
+    v[i] = 0.f;  // zero padding past the sequence end and past the last head
+    if (tok < L && h < H) v[i] = __ldg(dt + (b * L + tok) * H + h);
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid + 256 * i, t = e / kHeadsPerCta, k = e % kHeadsPerCta;
+    tile[k][t + t / 32] = v[i];
   }
   __syncthreads();
 
   const int64_t h = h0 + warp;
   if (h >= H) return;
   const float a = __ldg(A + h);
-  float d[R], run = 0.f;
+  float* out_cs = cs2 + ((b * H + h) * nc + c) * Q;
+  float* out_dt = dtT + ((b * H + h) * nc + c) * Q;
+  // round r covers tokens 32r .. 32r+31, one per lane: a warp-shuffle inclusive scan plus the
+  // running total of the earlier rounds; every store is one coalesced 128-byte row
+  float carry = 0.f;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int t = lane * R + r;
-    d[r] = tile[warp][t + t / 32];
-    run += a * d[r];
-    // keep the running in-lane prefix; the lane offset is added after the warp scan
-    tile[warp][t + t / 32] = run;
-  }
-  // inclusive warp scan of the lane totals
-  float incl = run;
+    const int t = 32 * r + lane;
+    const float d = tile[warp][t + t / 32];
+    float incl = a * d;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  const float excl = incl - run;
-  float* out_cs = cs2 + ((b * H + h) * nc + c) * Q + lane * R;
-  float* out_dt = dtT + ((b * H + h) * nc + c) * Q + lane * R;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int t = lane * R + r;
-    out_cs[r] = (excl + tile[warp][t + t / 32]) * kLog2e;
-    out_dt[r] = d[r];
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    out_cs[t] = (carry + incl) * kLog2e;
+    out_dt[t] = d;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 

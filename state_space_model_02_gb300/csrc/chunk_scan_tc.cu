@@ -7,19 +7,31 @@
 //              + 2^{cs2_i} (C_i . hprev[p,:]) + D_h x[i,p]
 // Three dense contractions run on tcgen05 with f32 accumulators in tensor memory (TMEM):
 //     CB = C_m B^T        (M = 128 rows i, N = j <= 256, K = state N)   once per (b, c, m-tile, group)
-//     Y1 = (L o CB) x_h   (M = 128, N = P = 64, K = j)                  per head
+//     Y1 = P x_h          (M = 128, N = P = 64, K = j)                  per head
 //     Y2 = C_m hprev_h^T  (M = 128, N = 64, K = state N)                per head
-// CB never leaves TMEM: for every head it is read back into registers, multiplied by the
-// decay mask L_ij = 2^{cs2_i - cs2_j} dt_j (j <= i, else 0), rounded to bf16 and written to
-// shared memory as Y1's A operand.  The mask is factored per 32-column block j0 as
+// with P = L o CB + D_h I: CB never leaves TMEM; for every head it is read back into registers,
+// multiplied by the decay mask L_ij = 2^{cs2_i - cs2_j} dt_j (j <= i, else 0), D_h is added on
+// the diagonal (so Y1 already holds D_h x_i), and the result is rounded to bf16 into shared
+// memory as Y1's A operand.  The mask is factored per 32-column block j0 as
 // 2^{cs2_i - cs2_j0} * (2^{cs2_j0 - cs2_j} dt_j): one exp2 per row per block plus a per-head
-// column table, and every factor stays inside float32 range (|cs2| per block <= 32*max(dt|A|)/ln2).
+// column table; every factor stays inside float32 range (|cs2| over 32 tokens <= 32*max|dt A|/ln2).
 //
-// Persistent CTAs (one per SM; 512 TMEM columns and ~210 KB shared memory each) walk a
+// Persistent CTAs (one per SM: 512 TMEM columns, ~214 KB shared memory, 14 warps) walk a
 // contiguous range of (batch, chunk, m-tile, head) units, weighted by the m-tile's causal
-// width; CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).
-// Per head, x and hprev arrive by TMA into one of two slots one head ahead, Y1/Y2 alternate
-// between two TMEM buffers, and the epilogue of head h-1 overlaps the MMAs of head h.
+// width; CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).  Warp
+// roles, synchronised through mbarriers so the kinds of work overlap across heads:
+//   warp 0      TMA producer: C and B per segment; per head hprev (2-slot ring, freed once Y2
+//               is done) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are done);
+//               it also warms L2 with the x and hprev tiles two heads ahead (TMA prefetch)
+//   warp 1      tcgen05.mma issuer; owns the TMEM allocation
+//   warps 2-9   mask: CB (TMEM) -> P (bf16, shared memory) for head h+1 ...
+//   warps 10-13 epilogue: ... while these finish head h: y = Y1 + 2^{cs2_i} Y2 -> TMA store
+// A warp reads the TMEM lane quarter (warp % 4): two mask warps share each quarter and take
+// alternate 32-column blocks; the four epilogue warps cover the 128 rows once.  P is handed to
+// the MMA issuer in four 64-column groups (one 16 KB swizzle atom each) with their own
+// barriers, so Y1's MMAs on group k overlap the mask writing group k+1.
+// Every wait is bounded; after an expiry all roles keep their loop trip counts (so named
+// barriers stay matched) but skip their work, then drain and release TMEM.
 // Requirements (chunk_scan_tc_ok): bf16 I/O, P = 64, Q in {128, 256}, N in {64, 128}.
 #include "ptx.cuh"
 #include "ssd_internal.h"
@@ -27,10 +39,13 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kMaskWarps = 8, kEpiWarps = 4;  // warps 2-9 mask, 10-13 epilogue
+constexpr int kWarps = 2 + kMaskWarps + kEpiWarps;
+constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kBox128 = 16384;  // TMA box: 128 rows x 128 bytes
 constexpr uint32_t kBox64 = 8192;    // TMA box: 64 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;  // CB [0,256) | Y1 buf0 | Y2 buf0 | Y1 buf1 | Y2 buf1
+constexpr uint32_t kBarMask = 1, kBarEpi = 2;  // named barriers of the mask and epilogue groups
 
 struct ScParams {
   int32_t L, H, nc, Q, N, hpg, MT;
@@ -38,7 +53,6 @@ struct ScParams {
   const float* cs2;
   const float* dtT;
   const float* D;
-  const uint16_t* x;
   uint32_t* status;
   uint64_t wait_ns;
 };
@@ -46,23 +60,32 @@ struct ScParams {
 template <int NB>  // NB = N / 64
 struct ScSmem {
   static constexpr uint32_t kC = 0;                          // NB x 16 KB: C rows of the m-tile
-  static constexpr uint32_t kP = kC + NB * kBox128;          // 64 KB: L o CB (bf16); B during CB phase
+  static constexpr uint32_t kP = kC + NB * kBox128;          // 64 KB: P (bf16); B during CB phase
   static constexpr uint32_t kPBytes = 65536;
-  static constexpr uint32_t kSlotX = 0;                      // 32 KB: x (up to 256 tokens x 64 p)
-  static constexpr uint32_t kSlotH = 32768;                  // NB x 8 KB: hprev (64 p x 64 n)
-  static constexpr uint32_t kSlotCs = kSlotH + NB * kBox64;  // 1 KB: cs2 row of the chunk
-  static constexpr uint32_t kSlotDt = kSlotCs + 1024;        // 1 KB: dt row of the chunk
-  static constexpr uint32_t kSlotBytes = kSlotDt + 1024;
-  static constexpr uint32_t kSlot0 = kP + kPBytes;
-  static constexpr uint32_t kY = kSlot0 + 2 * kSlotBytes;    // 16 KB: y staging (128 rows x 128 B)
-  static constexpr uint32_t kColf = kY + kBox128;            // 1 KB: per-head column factors
-  static constexpr uint32_t kBars = kColf + 1024;            // cb_full cb_done slot[2] y[2] drain
-  static constexpr uint32_t kTmemSlot = kBars + 8 * 8;
+  static constexpr uint32_t kHpBytes = NB * kBox64;          // hprev slot: 64 p x N (bf16)
+  static constexpr uint32_t kHp0 = kP + kPBytes;
+  static constexpr uint32_t kXsX = 0;                        // x slot: 32 KB x (up to 256 tokens x 64 p)
+  static constexpr uint32_t kXsCs = 32768;                   //         1 KB cs2 row of the chunk
+  static constexpr uint32_t kXsDt = kXsCs + 1024;            //         1 KB dt row of the chunk
+  static constexpr uint32_t kXsBytes = kXsDt + 1024;
+  static constexpr uint32_t kXs0 = kHp0 + 2 * kHpBytes;
+  static constexpr uint32_t kY = kXs0 + 2 * kXsBytes;        // 16 KB: y staging (128 rows x 128 B)
+  static constexpr uint32_t kColf = kY + kBox128;            // 2 x 1 KB: per-head column factors
+  static constexpr uint32_t kBars = kColf + 2048;
+  static constexpr int kNumBars = 26;
+  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kUsed = kAbort + 4;
   static constexpr uint32_t kAlloc = kUsed + 1024;           // slack for 1024-byte alignment
-  static_assert(kSlotBytes % 1024 == 0, "slots must stay 1024-byte aligned");
+  static_assert(kXsBytes % 1024 == 0 && kHpBytes % 1024 == 0, "slots must stay 1024-byte aligned");
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
+};
+
+// mbarrier indices
+enum : int {
+  kCbFull = 0, kCbDone, kCbEmpty, kSegFree, kHpFull0, kHpFull1, kHpEmpty0, kHpEmpty1,
+  kXsFull0, kXsFull1, kXsEmpty0, kXsEmpty1, kPFull0, kPEmpty0 = kPFull0 + 4,
+  kYFull0 = kPEmpty0 + 4, kYFull1, kYEmpty0, kYEmpty1, kDrain
 };
 
 // First unit whose starting weight is >= w.  Units are ordered (b, c, m-tile, h); a unit of
@@ -76,6 +99,25 @@ __device__ __forceinline__ int64_t unit_at_weight(int64_t w, int32_t H, int32_t 
   return h >= H ? (bc + 1) * 2 * H : bc * 2 * H + H + h;
 }
 
+// One run of consecutive heads sharing (b, c, m-tile, group): one CB.
+struct Segment {
+  int b, c, mt, g, h_begin, nh;
+};
+
+__device__ __forceinline__ Segment segment_at(int64_t u, int64_t u_end, const ScParams& prm) {
+  Segment s;
+  const int64_t bcm = u / prm.H;
+  s.h_begin = static_cast<int>(u % prm.H);
+  s.mt = static_cast<int>(bcm % prm.MT);
+  const int64_t bc = bcm / prm.MT;
+  s.c = static_cast<int>(bc % prm.nc);
+  s.b = static_cast<int>(bc / prm.nc);
+  s.g = s.h_begin / prm.hpg;
+  const int64_t h_end = min(int64_t((s.g + 1) * prm.hpg), s.h_begin + (u_end - u));
+  s.nh = static_cast<int>(h_end - s.h_begin);
+  return s;
+}
+
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -85,28 +127,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_y, const ScParams prm) {
   using SM = ScSmem<NB>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t H = prm.H, Q = prm.Q, N = prm.N, MT = prm.MT;
-
-  const uint32_t bar_cb_full = sb + SM::kBars, bar_cb_done = bar_cb_full + 8,
-                 bar_slot = bar_cb_full + 16, bar_y = bar_cb_full + 32, bar_drain = bar_cb_full + 48;
+  auto bar = [&](int i) { return sb + SM::kBars + 8u * i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlot);
-  float* colf = reinterpret_cast<float*>(smem + SM::kColf);
 
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_B);
     prefetch_tmap(&tm_C);
     prefetch_tmap(&tm_h);
     prefetch_tmap(&tm_y);
-    for (int i = 0; i < 7; ++i) mbar_init(bar_cb_full + 8 * i, 1);
+    const uint32_t counts[SM::kNumBars] = {
+        1, 1, kMaskWarps, 1,                                  // cb_full cb_done cb_empty seg_free
+        1, 1, 1, 1,                                           // hp_full[2] hp_empty[2]
+        1, 1, 1 + kMaskWarps, 1 + kMaskWarps,                 // xs_full[2] xs_empty[2]
+        kMaskWarps, kMaskWarps, kMaskWarps, kMaskWarps,       // p_full[4]
+        1, 1, 1, 1,                                           // p_empty[4]
+        1, 1, kEpiWarps, kEpiWarps,                           // y_full[2] y_empty[2]
+        1, 1};                                                // drain, spare
+    for (int i = 0; i < SM::kNumBars; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -115,114 +163,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_row = tmem + (uint32_t(warp * 32) << 16);
   const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
 
   const int64_t u_begin = unit_at_weight(prm.total_weight * blockIdx.x / gridDim.x, H, MT);
   const int64_t u_end = unit_at_weight(prm.total_weight * (blockIdx.x + 1) / gridDim.x, H, MT);
 
-  // thread-0 bookkeeping of TMA loads in flight, for the drain on abort
-  bool pend_cb = false, pend_slot[2] = {false, false};
-  uint32_t pend_cb_ph = 0, pend_slot_ph[2] = {0, 0};
-
-  uint32_t gi = 0, cb_phase = 0;
-  float e_keep = 0.f;
-
-  for (int64_t u = u_begin; u < u_end;) {
-    const int64_t bcm = u / H;
-    const int h_begin = static_cast<int>(u % H);
-    const int mt = static_cast<int>(bcm % MT);
-    const int64_t bc = bcm / MT;
-    const int c = static_cast<int>(bc % prm.nc), b = static_cast<int>(bc / prm.nc);
-    const int g = h_begin / prm.hpg;
-    const int h_end = static_cast<int>(min(int64_t((g + 1) * prm.hpg), h_begin + (u_end - u)));
-    const int nh = h_end - h_begin;
-    const int i0 = mt * 128, jrows = i0 + 128;
-    const int row = i0 + tid;                 // row of the chunk owned by this thread
-    const int nblk = jrows / 32, maxblk = i0 / 32 + warp;
-    const bool tile_live = int64_t(c) * Q + i0 < prm.L;  // any row of the m-tile inside [0, L)
-
-    auto load_head = [&](int hh, uint32_t k) {  // thread 0: x, hprev, cs2, dt of head hh -> slot
-      const uint32_t s = k & 1, ph = (k >> 1) & 1;
-      const uint32_t slot = sb + SM::kSlot0 + s * SM::kSlotBytes;
-      const uint32_t bar = bar_slot + 8 * s;
-      mbar_arrive_expect_tx(bar, jrows * 128 + NB * kBox64 + 2 * jrows * 4);
-      for (int jb = 0; jb < jrows / 128; ++jb)
-        tma_load_3d(slot + SM::kSlotX + jb * kBox128, &tm_x, bar, hh * 64, c * Q + jb * 128, b);
-      for (int nb = 0; nb < NB; ++nb)
-        tma_load_2d(slot + SM::kSlotH + nb * kBox64, &tm_h, bar, nb * 64,
-                    ((b * prm.nc + c) * H + hh) * 64);
-      const int64_t crow = ((int64_t(b) * H + hh) * prm.nc + c) * Q;
-      bulk_load(slot + SM::kSlotCs, prm.cs2 + crow, jrows * 4, bar);
-      bulk_load(slot + SM::kSlotDt, prm.dtT + crow, jrows * 4, bar);
-      pend_slot[s] = true;
-      pend_slot_ph[s] = ph;
-    };
-
-    // epilogue of head hh whose Y1/Y2 sit in TMEM buffer yb: y = Y1 + e*Y2 + D*x -> TMA store
-    auto epilogue = [&](int hh, uint32_t yb, float e) {
-      const int64_t t = int64_t(c) * Q + row;
-      const float Dh = prm.D ? __ldg(prm.D + hh) : 0.f;
-      uint4 xr[8];
-      if (t < prm.L) {
-        const uint4* xp = reinterpret_cast<const uint4*>(prm.x + ((int64_t(b) * prm.L + t) * H + hh) * 64);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xr[k] = __ldg(xp + k);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xr[k] = make_uint4(0, 0, 0, 0);
-      }
-      uint8_t* ys = smem + SM::kY + tid * 128;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32], q2[32];
-        __syncwarp();
-        tmem_ld32(tmem_row + 256 + 128 * yb + 32 * half, a);
-        tmem_ld32(tmem_row + 256 + 128 * yb + 64 + 32 * half, q2);
-        tmem_ld_wait();
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const uint4 xw = xr[4 * half + qq];
-          const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int k0 = 8 * qq + 2 * e2;
-            const float lo = __uint_as_float(a[k0]) + e * __uint_as_float(q2[k0]) + Dh * bf16lo_to_f32(xs[e2]);
-            const float hi = __uint_as_float(a[k0 + 1]) + e * __uint_as_float(q2[k0 + 1]) +
-                             Dh * bf16hi_to_f32(xs[e2]);
-            o[e2] = pack_bf16x2(lo, hi);
-          }
-          *reinterpret_cast<uint4*>(ys + (((4 * half + qq) ^ (tid & 7)) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0 && tile_live && !*abort_flag) {
-        tma_store_3d(&tm_y, sb + SM::kY, hh * 64, c * Q + i0, b);
-        bulk_commit();
-      }
-    };
-
-    // ---- segment start: operands of CB and the first two heads
-    if (tid == 0 && !*abort_flag) {
-      mbar_arrive_expect_tx(bar_cb_full, NB * kBox128 + NB * jrows * 128);
-      for (int nb = 0; nb < NB; ++nb)
-        tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar_cb_full, g * N + nb * 64, c * Q + i0, b);
-      for (int nb = 0; nb < NB; ++nb)
-        for (int jb = 0; jb < jrows / 128; ++jb)
-          tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar_cb_full,
-                      g * N + nb * 64, c * Q + jb * 128, b);
-      pend_cb = true;
-      pend_cb_ph = cb_phase;
-      for (int k = 0; k < 2 && k < nh; ++k) load_head(h_begin + k, gi + k);
-    }
-    if (tid == 0) {
-      if (mbar_wait(bar_cb_full, cb_phase, ctl)) {
-        pend_cb = false;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t gi = 0, si = 0;
+      bool pend_cb = false, pend_hp[2] = {false, false}, pend_xs[2] = {false, false};
+      uint32_t ph_cb = 0, ph_hp[2] = {0, 0}, ph_xs[2] = {0, 0};
+      for (int64_t u = u_begin; u < u_end; ++si) {
+        const Segment sg = segment_at(u, u_end, prm);
+        const int i0 = sg.mt * 128, jrows = i0 + 128;
+        // C and B of the new segment overwrite regions the previous segment's MMAs read
+        if (si >= 1) (void)mbar_wait(bar(kSegFree), (si - 1) & 1, ctl);
         if (!*abort_flag) {
+          mbar_arrive_expect_tx(bar(kCbFull), NB * kBox128 + NB * jrows * 128);
+          for (int nb = 0; nb < NB; ++nb)
+            tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + nb * 64,
+                        sg.c * Q + i0, sg.b);
+          for (int nb = 0; nb < NB; ++nb)
+            for (int jb = 0; jb < jrows / 128; ++jb)
+              tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar(kCbFull),
+                          sg.g * N + nb * 64, sg.c * Q + jb * 128, sg.b);
+          pend_cb = true;
+          ph_cb = si & 1;
+        }
+        for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+          const int hh = sg.h_begin + hi;
+          const uint32_t s = gi & 1, use = gi >> 1;
+          // hprev first: Y2 needs it first, and its slot frees early
+          if (gi >= 2) (void)mbar_wait(bar(kHpEmpty0 + s), (use - 1) & 1, ctl);
+          if (!*abort_flag) {
+            const uint32_t hb = bar(kHpFull0 + s);
+            mbar_arrive_expect_tx(hb, SM::kHpBytes);
+            for (int nb = 0; nb < NB; ++nb)
+              tma_load_2d(sb + SM::kHp0 + s * SM::kHpBytes + nb * kBox64, &tm_h, hb, nb * 64,
+                          ((sg.b * prm.nc + sg.c) * H + hh) * 64);
+            pend_hp[s] = true;
+            ph_hp[s] = use & 1;
+          }
+          if (gi >= 2) (void)mbar_wait(bar(kXsEmpty0 + s), (use - 1) & 1, ctl);
+          if (!*abort_flag) {
+            const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
+            const uint32_t xb = bar(kXsFull0 + s);
+            mbar_arrive_expect_tx(xb, jrows * 128 + 2 * jrows * 4);
+            for (int jb = 0; jb < jrows / 128; ++jb)
+              tma_load_3d(xs + SM::kXsX + jb * kBox128, &tm_x, xb, hh * 64, sg.c * Q + jb * 128, sg.b);
+            const int64_t crow = ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q;
+            bulk_load(xs + SM::kXsCs, prm.cs2 + crow, jrows * 4, xb);
+            bulk_load(xs + SM::kXsDt, prm.dtT + crow, jrows * 4, xb);
+            pend_xs[s] = true;
+            ph_xs[s] = use & 1;
+          }
+          // warm L2 with the x and hprev tiles of the unit two heads ahead
+          const int64_t up = u + hi + 2;
+          if (up < u_end && !*abort_flag) {
+            const Segment ps = segment_at(up, u_end, prm);
+            for (int jb = 0; jb <= ps.mt; ++jb)
+              tma_prefetch_3d(&tm_x, ps.h_begin * 64, ps.c * Q + jb * 128, ps.b);
+            for (int nb = 0; nb < NB; ++nb)
+              tma_prefetch_2d(&tm_h, nb * 64, ((ps.b * prm.nc + ps.c) * H + ps.h_begin) * 64);
+          }
+        }
+        u += sg.nh;
+      }
+      // drain: every load issued must have landed before the CTA may exit
+      if (pend_cb) (void)mbar_drain(bar(kCbFull), ph_cb, kWaitLimitNs);
+      for (int s = 0; s < 2; ++s) {
+        if (pend_hp[s]) (void)mbar_drain(bar(kHpFull0 + s), ph_hp[s], kWaitLimitNs);
+        if (pend_xs[s]) (void)mbar_drain(bar(kXsFull0 + s), ph_xs[s], kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t gi = 0, si = 0, gpar = 0;  // gpar bit k: parity of P group k's uses so far
+      for (int64_t u = u_begin; u < u_end; ++si) {
+        const Segment sg = segment_at(u, u_end, prm);
+        const int jrows = sg.mt * 128 + 128;
+        const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
+        const bool e = si == 0 || mbar_wait(bar(kCbEmpty), (si - 1) & 1, ctl);
+        if (a && e && !*abort_flag) {
           tc_fence_after();
           const uint32_t idesc = idesc_bf16_f32(128, jrows, 0, 0);
           for (int nb = 0; nb < NB; ++nb)
@@ -232,118 +256,204 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(sb + SM::kP + nb * jrows * 128 + k * 32, 16, 1024), idesc,
                        (nb | k) != 0 ? 1u : 0u);
         }
-      }
-      umma_commit(bar_cb_done);
-    }
-    (void)mbar_wait(bar_cb_done, cb_phase, ctl);
-    cb_phase ^= 1u;
-    tc_fence_after();
-    // blocks of P right of this warp's diagonal block stay zero for the whole segment
-    for (int blk = maxblk + 1; blk < nblk; ++blk) {
-      const int j0 = 32 * blk;
-      uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + tid * 128;
+        umma_commit(bar(kCbDone));
+        for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+          const uint32_t s = gi & 1, use = gi >> 1;
+          const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
+          const uint32_t hp = sb + SM::kHp0 + s * SM::kHpBytes;
+          const uint32_t ycol = 256 + 128 * s;
+          const bool h = mbar_wait(bar(kHpFull0 + s), use & 1, ctl);
+          const bool y = gi < 2 || mbar_wait(bar(kYEmpty0 + s), (use - 1) & 1, ctl);
+          if (h && y && !*abort_flag) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(pb + (((((j0 & 63) >> 3) + q) ^ (tid & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-    }
-
-    for (int hi = 0; hi < nh; ++hi, ++gi) {
-      const int h = h_begin + hi;
-      const uint32_t s = gi & 1, sph = (gi >> 1) & 1;
-      uint8_t* slotp = smem + SM::kSlot0 + s * SM::kSlotBytes;
-      const uint32_t slot = sb + SM::kSlot0 + s * SM::kSlotBytes;
-      if (hi >= 1) {
-        // MMAs of the previous head are done: its slot, the P tile and its TMEM buffer are free
-        const uint32_t pg = gi - 1;
-        (void)mbar_wait(bar_y + 8 * (pg & 1), (pg >> 1) & 1, ctl);
-        tc_fence_after();
-        if (tid == 0 && hi + 1 < nh && !*abort_flag) load_head(h + 1, gi + 1);
-      }
-      const bool have = mbar_wait(bar_slot + 8 * s, sph, ctl);
-      if (tid == 0 && have) pend_slot[s] = false;
-      const float* cs = reinterpret_cast<const float*>(slotp + SM::kSlotCs);
-      const float* dtv = reinterpret_cast<const float*>(slotp + SM::kSlotDt);
-      for (int j = tid; j < jrows; j += kThreads) colf[j] = ex2(cs[j & ~31] - cs[j]) * dtv[j];
-      const float cs_i = cs[row];
-      __syncthreads();
-      if (tid == 0 && !*abort_flag) {
-        tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_f16(tmem + 256 + 128 * s + 64, sdesc_sw128(sb + SM::kC + nb * kBox128 + k * 32, 16, 1024),
-                     sdesc_sw128(slot + SM::kSlotH + nb * kBox64 + k * 32, 16, 1024), idesc,
-                     (nb | k) != 0 ? 1u : 0u);
-      }
-      // L o CB for this head -> P (bf16, K-major, 128-byte swizzle)
-      for (int blk = 0; blk <= maxblk && blk < nblk; ++blk) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(tmem_row + 32 * blk, v);
-        tmem_ld_wait();
-        const int j0 = 32 * blk;
-        const float rowf = ex2(cs_i - cs[j0]);
-        const bool diag = blk == maxblk;
-        uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + tid * 128;
-        const int cbase = (j0 & 63) >> 3;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t o[4];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int k0 = 8 * q + 2 * e2;
-            float lo = __uint_as_float(v[k0]) * colf[j0 + k0] * rowf;
-            float hi = __uint_as_float(v[k0 + 1]) * colf[j0 + k0 + 1] * rowf;
-            if (diag && j0 + k0 > row) lo = 0.f;
-            if (diag && j0 + k0 + 1 > row) hi = 0.f;
-            o[e2] = pack_bf16x2(lo, hi);
+              for (int k = 0; k < 4; ++k)
+                umma_f16(tmem + ycol + 64, sdesc_sw128(sb + SM::kC + nb * kBox128 + k * 32, 16, 1024),
+                         sdesc_sw128(hp + nb * kBox64 + k * 32, 16, 1024), idesc, (nb | k) != 0 ? 1u : 0u);
           }
-          *reinterpret_cast<uint4*>(pb + (((cbase + q) ^ (tid & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          umma_commit(bar(kHpEmpty0 + s));
+          const bool f = mbar_wait(bar(kXsFull0 + s), use & 1, ctl);
+          const uint32_t idesc1 = idesc_bf16_f32(128, 64, 0, 1);
+          for (int k = 0; k < jrows / 64; ++k) {
+            const bool p = mbar_wait(bar(kPFull0 + k), (gpar >> k) & 1u, ctl);
+            if (f && y && p && !*abort_flag) {
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16(tmem + ycol, sdesc_sw128(sb + SM::kP + k * kBox128 + kk * 32, 16, 1024),
+                         sdesc_sw128(xs + SM::kXsX + (4 * k + kk) * 2048, kBox128, 1024), idesc1,
+                         (k | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(bar(kPEmpty0 + k));
+            gpar ^= 1u << k;
+          }
+          umma_commit(bar(kYFull0 + s));
+          umma_commit(bar(kXsEmpty0 + s));
         }
+        umma_commit(bar(kSegFree));
+        u += sg.nh;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      if (tid == 0) bulk_wait_read0();  // the y staging buffer is free for the epilogue below
-      __syncthreads();
-      if (tid == 0) {
-        if (!*abort_flag) {
-          tc_fence_after();
-          const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
-          for (int k = 0; k < jrows / 16; ++k)
-            umma_f16(tmem + 256 + 128 * s, sdesc_sw128(sb + SM::kP + (k >> 2) * kBox128 + (k & 3) * 32, 16, 1024),
-                     sdesc_sw128(slot + SM::kSlotX + k * 2048, kBox128, 1024), idesc, k != 0 ? 1u : 0u);
-        }
-        umma_commit(bar_y + 8 * s);
-      }
-      const float e_cur = ex2(cs_i);
-      if (hi >= 1) epilogue(h - 1, (gi - 1) & 1, e_keep);
-      e_keep = e_cur;
+      umma_commit(bar(kDrain));
+      (void)mbar_drain(bar(kDrain), 0, kWaitLimitNs);
     }
-    // drain the segment: last head's epilogue
-    {
-      const uint32_t lg = gi - 1;
-      (void)mbar_wait(bar_y + 8 * (lg & 1), (lg >> 1) & 1, ctl);
+  } else if (warp < 2 + kMaskWarps) {
+    // ------------------------------------------------------------- mask: CB -> P in smem
+    const int q = warp & 3, r = 32 * q + lane;  // TMEM lane quarter and m-tile row
+    const int sub = (warp - 2) >> 2;            // which of the quarter's two mask warps
+    const int mt_thread = (warp - 2) * 32 + lane;  // 0..255 over the mask group
+    const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
+    uint32_t gi = 0, si = 0;
+    uint32_t gpar = 0, gused = 0;  // per P group: parity of its uses so far, used at least once
+    for (int64_t u = u_begin; u < u_end; ++si) {
+      const Segment sg = segment_at(u, u_end, prm);
+      const int i0 = sg.mt * 128, jrows = i0 + 128, row = i0 + r;
+      const int nblk = jrows / 32, maxblk = i0 / 32 + q;
+      (void)mbar_wait(bar(kCbDone), si & 1, ctl);
       tc_fence_after();
-      if (tid == 0) bulk_wait_read0();
-      __syncthreads();
-      epilogue(h_end - 1, lg & 1, e_keep);
+      // blocks right of this quarter's diagonal block stay zero for the whole segment
+      for (int blk = maxblk + 1 + sub; blk < nblk; blk += 2) {
+        const int j0 = 32 * blk;
+        uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + r * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(pb + (((((j0 & 63) >> 3) + c4) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+      }
+      for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+        const uint32_t s = gi & 1;
+        const uint8_t* xsp = smem + SM::kXs0 + s * SM::kXsBytes;
+        const float* cs = reinterpret_cast<const float*>(xsp + SM::kXsCs);
+        const float* dtv = reinterpret_cast<const float*>(xsp + SM::kXsDt);
+        float* colf = reinterpret_cast<float*>(smem + SM::kColf + (gi & 1) * 1024);
+        const bool have = mbar_wait(bar(kXsFull0 + s), (gi >> 1) & 1, ctl);
+        if (have && mt_thread < jrows)
+          colf[mt_thread] = ex2(cs[mt_thread & ~31] - cs[mt_thread]) * dtv[mt_thread];
+        const float cs_i = have ? cs[row] : 0.f;
+        const float Dh = prm.D ? __ldg(prm.D + sg.h_begin + hi) : 0.f;
+        named_bar_sync(kBarMask, 32 * kMaskWarps);
+        const bool live = have && !*abort_flag;
+        tc_fence_after();
+        // group k holds 32-column blocks 2k and 2k+1; this warp owns block 2k + sub.  The TMEM
+        // load of the block is issued before the wait for the group's P buffer.
+        const int ng = jrows / 64;
+#pragma unroll 1
+        for (int k = 0; k < ng; ++k) {
+          const int blk = 2 * k + sub, j0 = 32 * blk;
+          const bool mine = live && blk <= maxblk;
+          uint32_t v[32];
+          if (mine) {
+            __syncwarp();
+            tmem_ld32(trow + j0, v);
+          }
+          const bool pfree = !((gused >> k) & 1u) || mbar_wait(bar(kPEmpty0 + k), ((gpar >> k) & 1u) ^ 1u, ctl);
+          if (mine) tmem_ld_wait();
+          if (mine && pfree) {
+            // P[row, j] = CB[row, j] colf[j] 2^(cs2_row - cs2_j0), zero right of the diagonal,
+            // plus D_h on it
+            const float rowf = ex2(cs_i - cs[j0]);
+            const float2 rf = make_float2(rowf, rowf);
+            const bool diag = blk == maxblk;
+            const float4* cf = reinterpret_cast<const float4*>(colf + j0);
+            uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + r * 128;
+            const int cbase = (j0 & 63) >> 3;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 fa = cf[2 * c4], fb = cf[2 * c4 + 1];
+              const float2 f2[4] = {make_float2(fa.x, fa.y), make_float2(fa.z, fa.w), make_float2(fb.x, fb.y),
+                                    make_float2(fb.z, fb.w)};
+              uint32_t o[4];
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int e = 8 * c4 + 2 * e2;
+                float2 w = mul_f32x2(mul_f32x2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2[e2]), rf);
+                if (diag) {
+                  w.x = j0 + e > row ? 0.f : (j0 + e == row ? w.x + Dh : w.x);
+                  w.y = j0 + e + 1 > row ? 0.f : (j0 + e + 1 == row ? w.y + Dh : w.y);
+                }
+                o[e2] = pack_bf16x2(w.x, w.y);
+              }
+              *reinterpret_cast<uint4*>(pb + (((cbase + c4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kPFull0 + k));
+          gpar ^= 1u << k;
+          gused |= 1u << k;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kXsEmpty0 + s));
+      }
+      // CB of this segment has been read for the last time
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kCbEmpty));
+      u += sg.nh;
     }
-    u += nh;
+  } else {
+    // ------------------------ epilogue: y = Y1 + 2^cs2_i Y2 -> staging -> TMA store of y
+    // (D x already sits in Y1 through P's diagonal)
+    const int q = warp & 3, r = 32 * q + lane;
+    const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
+    const bool store_thread = warp == 2 + kMaskWarps && lane == 0;
+    uint32_t gi = 0;
+    for (int64_t u = u_begin; u < u_end;) {
+      const Segment sg = segment_at(u, u_end, prm);
+      const int i0 = sg.mt * 128, row = i0 + r;
+      const bool tile_live = int64_t(sg.c) * Q + i0 < prm.L;
+      for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+        const int hh = sg.h_begin + hi;
+        const uint32_t s = gi & 1;
+        // this row's cs2 (one coalesced L2 read per warp), fetched while the MMAs finish
+        const float cs_i = __ldg(prm.cs2 + ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q + row);
+        const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && !*abort_flag;
+        tc_fence_after();
+        if (store_thread) bulk_wait_read0();  // the staging buffer is free again
+        named_bar_sync(kBarEpi, 32 * kEpiWarps);
+        if (ok) {
+          const float e = ex2(cs_i);
+          uint8_t* ys = smem + SM::kY + r * 128;
+#pragma unroll
+          for (int quarter = 0; quarter < 4; ++quarter) {
+            uint32_t a[16], q2[16];
+            __syncwarp();
+            tmem_ld16(trow + 256 + 128 * s + 16 * quarter, a);
+            tmem_ld16(trow + 256 + 128 * s + 64 + 16 * quarter, q2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int cc = 2 * quarter + c2;
+              uint32_t o[4];
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int k0 = 8 * c2 + 2 * e2;
+                o[e2] = pack_bf16x2(__uint_as_float(a[k0]) + e * __uint_as_float(q2[k0]),
+                                    __uint_as_float(a[k0 + 1]) + e * __uint_as_float(q2[k0 + 1]));
+              }
+              *reinterpret_cast<uint4*>(ys + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kYEmpty0 + s));
+        fence_proxy_async_smem();
+        named_bar_sync(kBarEpi, 32 * kEpiWarps);
+        if (store_thread && ok && tile_live) {
+          tma_store_3d(&tm_y, sb + SM::kY, hh * 64, sg.c * Q + i0, sg.b);
+          bulk_commit();
+        }
+      }
+      u += sg.nh;
+    }
+    if (store_thread) bulk_wait_read0();  // the stores have read the staging buffer
   }
 
-  // teardown: drain whatever is still in flight, then release tensor memory
-  if (tid == 0) {
-    if (pend_cb) (void)mbar_drain(bar_cb_full, pend_cb_ph, kWaitLimitNs);
-    for (int s = 0; s < 2; ++s)
-      if (pend_slot[s]) (void)mbar_drain(bar_slot + 8 * s, pend_slot_ph[s], kWaitLimitNs);
-    umma_commit(bar_drain);
-    (void)mbar_drain(bar_drain, 0, kWaitLimitNs);
-    bulk_wait0();
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -405,7 +515,6 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   prm.cs2 = cs2;
   prm.dtT = dtT;
   prm.D = D;
-  prm.x = static_cast<const uint16_t*>(x);
   prm.status = status;
   prm.wait_ns = kWaitLimitNs;
   int sms = num_sms_current_device();

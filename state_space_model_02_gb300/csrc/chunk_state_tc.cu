@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_S, const CsParams prm) {
   using SM = CsSmem<NT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(bar_drain);
       (void)mbar_drain(bar_drain, 0, kWaitLimitNs);
     }
-    bulk_wait0();
+    bulk_wait_read0();  // shared memory may be released once the stores have read it
   }
   tc_fence_before();
   __syncthreads();

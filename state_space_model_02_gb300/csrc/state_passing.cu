@@ -29,7 +29,7 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
 }
 
 template <typename HT>
-__global__ void __launch_bounds__(256) state_passing_vec4_kernel(
+__global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
     const float* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
     int64_t Q, int64_t total4) {
@@ -39,35 +39,42 @@ __global__ void __launch_bounds__(256) state_passing_vec4_kernel(
   const int64_t bh = idx / per_bh, e = (idx % per_bh) * 4;
   const int64_t bi = bh / H, h = bh % H;
   const int64_t cstride = H * PN;  // elements between chunks in S / hprev
-  const float* Sp = S + (bi * nc * H + h) * PN + e;
   HT* Hp = hprev + (bi * nc * H + h) * PN + e;
-  const float* dec = cs2 + bh * nc * Q + (Q - 1);
+  const int n = static_cast<int>(nc);
 
   float4 hv = init ? __ldg(reinterpret_cast<const float4*>(init + bh * PN + e))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 sbuf[kDepth];
   float dbuf[kDepth];
+  // prologue: the first kDepth chunks in flight; pointers advance one chunk per load
+  const float* sp = S + (bi * nc * H + h) * PN + e;
+  const float* dp = cs2 + bh * nc * Q + (Q - 1);
 #pragma unroll
   for (int k = 0; k < kDepth; ++k) {
-    if (k < nc) {
-      sbuf[k] = __ldcs(reinterpret_cast<const float4*>(Sp + k * cstride));
-      dbuf[k] = __ldg(dec + k * Q);
+    if (k < n) {
+      sbuf[k] = __ldcs(reinterpret_cast<const float4*>(sp));
+      dbuf[k] = __ldg(dp);
+      sp += cstride;
+      dp += Q;
     }
   }
-  for (int64_t c0 = 0; c0 < nc; c0 += kDepth) {
+  for (int c0 = 0; c0 < n; c0 += kDepth) {
 #pragma unroll
     for (int k = 0; k < kDepth; ++k) {
-      const int64_t c = c0 + k;
-      if (c < nc) {
-        store4(Hp + c * cstride, hv);
+      const int c = c0 + k;
+      if (c < n) {
+        store4(Hp, hv);
+        Hp += cstride;
         const float d = ex2(dbuf[k]);
         hv.x = fmaf(d, hv.x, sbuf[k].x);
         hv.y = fmaf(d, hv.y, sbuf[k].y);
         hv.z = fmaf(d, hv.z, sbuf[k].z);
         hv.w = fmaf(d, hv.w, sbuf[k].w);
-        if (c + kDepth < nc) {
-          sbuf[k] = __ldcs(reinterpret_cast<const float4*>(Sp + (c + kDepth) * cstride));
-          dbuf[k] = __ldg(dec + (c + kDepth) * Q);
+        if (c + kDepth < n) {  // refill this ring entry with chunk c + kDepth
+          sbuf[k] = __ldcs(reinterpret_cast<const float4*>(sp));
+          dbuf[k] = __ldg(dp);
+          sp += cstride;
+          dp += Q;
         }
       }
     }
