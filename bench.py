@@ -57,8 +57,8 @@ def algorithmic(shape):
     cs = b * H * nc * Q * 4                      # bytes of one cs2 / dtT array
     by = {
         "chunk_cumsum": b * L * H * 4 + H * 4 + 2 * cs,
-        "chunk_state": b * L * H * P * e + b * L * G * N * e + 2 * cs + st * 4,
-        "state_passing": st * 4 + b * H * nc * 4 + st * e + 2 * b * H * P * N * 4,
+        "chunk_state": b * L * H * P * e + b * L * G * N * e + 2 * cs + st * e,
+        "state_passing": st * e + b * H * nc * 4 + st * e + 2 * b * H * P * N * 4,
         "chunk_scan": 2 * b * L * H * P * e + 2 * b * L * G * N * e + 2 * cs + st * e + H * 4,
     }
     fl = {

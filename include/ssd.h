@@ -77,7 +77,8 @@ typedef struct {
  *   cs2   float32 (b, H, nc, Q): log2(e) * in-chunk inclusive cumsum of A*dt,
  *         zero-padded past seqlen (chunk_cumsum output)
  *   dtT   float32 (b, H, nc, Q): dt laid out per head and chunk, zero-padded
- *   S     float32 (b, nc, H, P, N): per-chunk end state started from zero
+ *   S     (b, nc, H, P, N): per-chunk end state started from zero; bfloat16
+ *         when io_dtype is SSD_BF16, float32 when SSD_F32
  *   hprev (b, nc, H, P, N): state entering each chunk; bfloat16 when
  *         io_dtype is SSD_BF16, float32 when SSD_F32
  *   status uint32 at offset 0: 0, or an ssd_status recorded by a kernel      */

@@ -14,7 +14,7 @@
 //   thread 0 issues TMA loads (2-stage ring over 64-token k-blocks) and the MMAs;
 //   all threads scale the x tile in shared memory by the per-token decay weight
 //   (one scale per 128-byte row, so the swizzle is irrelevant), then drain the f32
-//   accumulator from tensor memory and stage it for TMA stores of S.
+//   accumulator from tensor memory and stage it, rounded to bf16, for TMA stores of S.
 // Requirements (checked by chunk_state_tc_ok): bf16 I/O, P = 64, Q in {128, 256},
 // N in {64, 128, 256, 512} (512 runs as two 256-wide n-tiles).
 #include "ptx.cuh"
@@ -46,8 +46,7 @@ struct CsSmem {
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kUsed = kAbort + 4;
   static constexpr uint32_t kAlloc = kUsed + 1024;    // slack for 1024-byte alignment
-  static constexpr uint32_t kEpiCols = NT < 128 ? NT : 128;
-  static_assert(4 * 2 * kBox <= kTiles || NT == 64, "epilogue staging must fit in the ring");
+  static_assert((NT / 64) * 2 * kBox <= kTiles, "epilogue staging must fit in the ring");
 };
 
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
@@ -181,34 +180,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   if (acc_ok) {
-    constexpr int kEpi = SM::kEpiCols;
-    for (int half = 0; half < NT / kEpi; ++half) {
-      if (half > 0) {
-        if (tid == 0) bulk_wait_read0();
-        __syncthreads();
-      }
-      const int k = tid >> 6, r = tid & 63;
+    // S is stored in bf16: one 64 x 64 box (8 KB, 128-byte rows, swizzled) per (n block, head)
+    const int k = tid >> 6, r = tid & 63;
 #pragma unroll 1
-      for (int q = 0; q < kEpi / 32; ++q) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + half * kEpi + q * 32, v);
-        tmem_ld_wait();
-        uint8_t* box = smem + (q * 2 + k) * kBox;
+    for (int q = 0; q < NT / 32; ++q) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + q * 32, v);
+      tmem_ld_wait();
+      uint8_t* box = smem + ((q >> 1) * 2 + k) * kBox;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(box + r * 128 + ((cc ^ (r & 7)) << 4)) =
-              make_uint4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int cc = (q & 1) * 4 + c4;
+        *reinterpret_cast<uint4*>(box + r * 128 + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(pack_bf16x2(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
       }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        for (int q = 0; q < kEpi / 32; ++q)
-          for (int kk = 0; kk < nh; ++kk)
-            tma_store_2d(&tm_S, sb + (q * 2 + kk) * kBox, nt * NT + half * kEpi + q * 32,
-                         ((b * prm.nc + c) * prm.H + h0 + kk) * 64);
-        bulk_commit();
-      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      for (int j = 0; j < NT / 64; ++j)
+        for (int kk = 0; kk < nh; ++kk)
+          tma_store_2d(&tm_S, sb + (j * 2 + kk) * kBox, nt * NT + j * 64,
+                       ((b * prm.nc + c) * prm.H + h0 + kk) * 64);
+      bulk_commit();
     }
   }
 
@@ -253,7 +251,7 @@ bool chunk_state_tc_ok(const Problem& p) {
 }
 
 cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
-                                  const float* dtT, float* S, uint32_t* status, cudaStream_t st,
+                                  const float* dtT, void* S, uint32_t* status, cudaStream_t st,
                                   const char** why) {
   const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
   CUtensorMap tx, tb, ts;
@@ -275,9 +273,9 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
   }
   {
     const uint64_t dims[2] = {uint64_t(p.N), uint64_t(p.b * p.nc * p.H * p.P)};
-    const uint64_t strides[1] = {uint64_t(p.N * 4)};
-    const uint32_t box[2] = {32, 64};
-    if (!encode_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S, dims, strides, box,
+    const uint64_t strides[1] = {uint64_t(p.N * 2)};
+    const uint32_t box[2] = {64, 64};
+    if (!encode_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, S, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }

@@ -33,7 +33,7 @@ constexpr int T = 32;  // tile edge
 template <typename IO>
 __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const float* __restrict__ cs2,
-    const float* __restrict__ dtT, float* __restrict__ S, int64_t L, int64_t H, int64_t P,
+    const float* __restrict__ dtT, IO* __restrict__ S, int64_t L, int64_t H, int64_t P,
     int64_t N, int64_t G, int64_t Q, int64_t nc) {
   __shared__ float xs[T][T + 1];
   __shared__ float bs[T][T + 1];
@@ -69,11 +69,11 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
     }
     __syncthreads();
   }
-  float* out = S + (((b * nc + c) * H + h) * P) * N;
+  IO* out = S + (((b * nc + c) * H + h) * P) * N;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int64_t p = p0 + ty + 8 * k, n = n0 + tx;
-    if (p < P && n < N) out[p * N + n] = acc[k];
+    if (p < P && n < N) st_io(out, p * N + n, acc[k]);
   }
 }
 
@@ -183,18 +183,19 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
 }  // namespace
 
 cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void* B, const float* cs2,
-                                    const float* dtT, float* S, cudaStream_t st) {
+                                    const float* dtT, void* S, cudaStream_t st) {
   const int64_t tiles = ((p.P + T - 1) / T) * ((p.N + T - 1) / T);
   const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.H),
                   static_cast<unsigned>(p.b * p.nc));
   if (p.io_bf16)
     chunk_state_simt_kernel<uint16_t><<<grid, 256, 0, st>>>(
-        static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(B), cs2, dtT, S, p.L, p.H,
-        p.P, p.N, p.G, p.Q, p.nc);
+        static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(B), cs2, dtT,
+        static_cast<uint16_t*>(S), p.L, p.H, p.P, p.N, p.G, p.Q, p.nc);
   else
     chunk_state_simt_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x),
-                                                         static_cast<const float*>(B), cs2, dtT, S,
-                                                         p.L, p.H, p.P, p.N, p.G, p.Q, p.nc);
+                                                         static_cast<const float*>(B), cs2, dtT,
+                                                         static_cast<float*>(S), p.L, p.H, p.P, p.N,
+                                                         p.G, p.Q, p.nc);
   return cudaGetLastError();
 }
 

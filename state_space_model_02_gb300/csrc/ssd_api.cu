@@ -61,7 +61,7 @@ struct Views {
   uint32_t* status;
   float* cs2;
   float* dtT;
-  float* S;
+  void* S;  // per-chunk states, in the I/O dtype
   void* hprev;
 };
 
@@ -75,7 +75,7 @@ ssd_status carve(const ssd::Problem& p, void* ws, size_t ws_bytes, Views* v) {
   v->status = reinterpret_cast<uint32_t*>(base + l.status);
   v->cs2 = reinterpret_cast<float*>(base + l.cs2);
   v->dtT = reinterpret_cast<float*>(base + l.dtT);
-  v->S = reinterpret_cast<float*>(base + l.S);
+  v->S = base + l.S;
   v->hprev = base + l.hprev;
   return SSD_OK;
 }

@@ -32,7 +32,7 @@ inline Layout make_layout(const Problem& p) {
   l.cs2 = 1024;
   l.dtT = align_up(l.cs2 + cs_bytes, 1024);
   l.S = align_up(l.dtT + cs_bytes, 1024);
-  l.hprev = align_up(l.S + st_elems * 4u, 1024);
+  l.hprev = align_up(l.S + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
   l.total = align_up(l.hprev + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
   return l;
 }
@@ -45,12 +45,12 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
                                 float* dtT, cudaStream_t st);
 
-cudaError_t launch_state_passing(const Problem& p, const float* S, const float* cs2,
+cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,
                                  cudaStream_t st);
 
 cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void* B, const float* cs2,
-                                    const float* dtT, float* S, cudaStream_t st);
+                                    const float* dtT, void* S, cudaStream_t st);
 
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
@@ -61,7 +61,7 @@ bool chunk_state_tc_ok(const Problem& p);
 bool chunk_scan_tc_ok(const Problem& p);
 
 cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
-                                  const float* dtT, float* S, uint32_t* status, cudaStream_t st,
+                                  const float* dtT, void* S, uint32_t* status, cudaStream_t st,
                                   const char** why);
 
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,

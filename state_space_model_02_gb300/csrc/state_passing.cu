@@ -10,8 +10,9 @@
 // chunk_cumsum row; zero padding past the sequence end leaves it unchanged).
 //
 // The loop over chunks is a dependent FMA chain per element, so the kernel is bound by HBM
-// latency x bandwidth: each thread owns 4 consecutive state elements (one float4 of S per
-// chunk) and keeps kDepth chunks of S in flight in registers ahead of the chain.
+// latency x bandwidth: each thread owns 4 consecutive state elements (4 values of S per
+// chunk, stored in the I/O dtype) and keeps kDepth chunks of S in flight in registers ahead of
+// the chain.  The chain itself runs in float32.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -21,6 +22,15 @@ namespace {
 constexpr int kDepth = 8;
 
 __device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ float4 load4(const float* src) { return __ldcs(reinterpret_cast<const float4*>(src)); }
+__device__ __forceinline__ float4 load4(const uint16_t* src) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(src));
+  return make_float4(bf16lo_to_f32(u.x), bf16hi_to_f32(u.x), bf16lo_to_f32(u.y), bf16hi_to_f32(u.y));
+}
+__device__ __forceinline__ float load1(const float* src) { return __ldg(src); }
+__device__ __forceinline__ float load1(const uint16_t* src) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(src)) << 16);
+}
 __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
   uint2 u;
   u.x = pack_bf16x2(v.x, v.y);
@@ -30,7 +40,7 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
 
 template <typename HT>
 __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
-    const float* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
+    const HT* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
     int64_t Q, int64_t total4) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -47,12 +57,12 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
   float4 sbuf[kDepth];
   float dbuf[kDepth];
   // prologue: the first kDepth chunks in flight; pointers advance one chunk per load
-  const float* sp = S + (bi * nc * H + h) * PN + e;
+  const HT* sp = S + (bi * nc * H + h) * PN + e;
   const float* dp = cs2 + bh * nc * Q + (Q - 1);
 #pragma unroll
   for (int k = 0; k < kDepth; ++k) {
     if (k < n) {
-      sbuf[k] = __ldcs(reinterpret_cast<const float4*>(sp));
+      sbuf[k] = load4(sp);
       dbuf[k] = __ldg(dp);
       sp += cstride;
       dp += Q;
@@ -71,7 +81,7 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
         hv.z = fmaf(d, hv.z, sbuf[k].z);
         hv.w = fmaf(d, hv.w, sbuf[k].w);
         if (c + kDepth < n) {  // refill this ring entry with chunk c + kDepth
-          sbuf[k] = __ldcs(reinterpret_cast<const float4*>(sp));
+          sbuf[k] = load4(sp);
           dbuf[k] = __ldg(dp);
           sp += cstride;
           dp += Q;
@@ -90,7 +100,7 @@ __device__ __forceinline__ void store1(uint16_t* dst, float v) {
 // Any P*N: one element per thread, no vectorisation.
 template <typename HT>
 __global__ void __launch_bounds__(256) state_passing_scalar_kernel(
-    const float* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
+    const HT* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
     int64_t Q, int64_t total) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -98,20 +108,20 @@ __global__ void __launch_bounds__(256) state_passing_scalar_kernel(
   const int64_t bh = idx / PN, e = idx % PN;
   const int64_t bi = bh / H, h = bh % H;
   const int64_t cstride = H * PN;
-  const float* Sp = S + (bi * nc * H + h) * PN + e;
+  const HT* Sp = S + (bi * nc * H + h) * PN + e;
   HT* Hp = hprev + (bi * nc * H + h) * PN + e;
   const float* dec = cs2 + bh * nc * Q + (Q - 1);
   float hv = init ? __ldg(init + bh * PN + e) : 0.f;
   for (int64_t c = 0; c < nc; ++c) {
     store1(Hp + c * cstride, hv);
-    hv = fmaf(ex2(__ldg(dec + c * Q)), hv, __ldg(Sp + c * cstride));
+    hv = fmaf(ex2(__ldg(dec + c * Q)), hv, load1(Sp + c * cstride));
   }
   if (final_state) final_state[bh * PN + e] = hv;
 }
 
 }  // namespace
 
-cudaError_t launch_state_passing(const Problem& p, const float* S, const float* cs2,
+cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,
                                  cudaStream_t st) {
   const int64_t PN = p.P * p.N;
@@ -121,17 +131,17 @@ cudaError_t launch_state_passing(const Problem& p, const float* S, const float* 
   if (vec) {
     if (p.io_bf16)
       state_passing_vec4_kernel<uint16_t><<<blocks, 256, 0, st>>>(
-          S, cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+          static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
       state_passing_vec4_kernel<float><<<blocks, 256, 0, st>>>(
-          S, cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+          static_cast<const float*>(S), cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   } else {
     if (p.io_bf16)
       state_passing_scalar_kernel<uint16_t><<<blocks, 256, 0, st>>>(
-          S, cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+          static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
       state_passing_scalar_kernel<float><<<blocks, 256, 0, st>>>(
-          S, cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+          static_cast<const float*>(S), cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   }
   return cudaGetLastError();
 }

@@ -237,7 +237,7 @@ def intermediates(prob: Problem, workspace):
 
     cs2 = view(lay.cs2, b * H * nc * Q, torch.float32, (b, H, nc, Q))
     dtT = view(lay.dtT, b * H * nc * Q, torch.float32, (b, H, nc, Q))
-    S = view(lay.S, b * nc * H * P * N, torch.float32, (b, nc, H, P, N))
     hdt = torch.bfloat16 if prob.io_dtype == SSD_BF16 else torch.float32
+    S = view(lay.S, b * nc * H * P * N, hdt, (b, nc, H, P, N))
     hprev = view(lay.hprev, b * nc * H * P * N, hdt, (b, nc, H, P, N))
     return cs2, dtT, S, hprev
