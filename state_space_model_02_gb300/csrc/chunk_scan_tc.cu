@@ -21,8 +21,9 @@
 // width; CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).  Warp
 // roles, synchronised through mbarriers so the kinds of work overlap across heads:
 //   warp 0      TMA producer: C and B per segment; per head hprev (2-slot ring, freed once Y2
-//               is done) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are done);
-//               it also warms L2 with the x and hprev tiles two heads ahead (TMA prefetch)
+//               is done; one box) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are
+//               done).  A TMA box costs the SM about the same for 64 or 128 rows, so operands
+//               come in few, large boxes and nothing is prefetched separately;
 //   warp 1      tcgen05.mma issuer; owns the TMEM allocation
 //   warps 2-9   mask: CB (TMEM) -> P (bf16, shared memory) for head h+1 ...
 //   warps 10-13 epilogue: ... while these finish head h: y = Y1 + 2^{cs2_i} Y2 -> TMA store
@@ -199,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!*abort_flag) {
             const uint32_t hb = bar(kHpFull0 + s);
             mbar_arrive_expect_tx(hb, SM::kHpBytes);
-            for (int nb = 0; nb < NB; ++nb)
-              tma_load_2d(sb + SM::kHp0 + s * SM::kHpBytes + nb * kBox64, &tm_h, hb, nb * 64,
-                          ((sg.b * prm.nc + sg.c) * H + hh) * 64);
+            // one 3-D box brings both 64-column halves of the head's state (NB 8 KB tiles)
+            tma_load_3d(sb + SM::kHp0 + s * SM::kHpBytes, &tm_h, hb, 0,
+                        ((sg.b * prm.nc + sg.c) * H + hh) * 64, 0);
             pend_hp[s] = true;
             ph_hp[s] = use & 1;
           }
@@ -217,15 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(xs + SM::kXsDt, prm.dtT + crow, jrows * 4, xb);
             pend_xs[s] = true;
             ph_xs[s] = use & 1;
-          }
-          // warm L2 with the x and hprev tiles of the unit two heads ahead
-          const int64_t up = u + hi + 2;
-          if (up < u_end && !*abort_flag) {
-            const Segment ps = segment_at(up, u_end, prm);
-            for (int jb = 0; jb <= ps.mt; ++jb)
-              tma_prefetch_3d(&tm_x, ps.h_begin * 64, ps.c * Q + jb * 128, ps.b);
-            for (int nb = 0; nb < NB; ++nb)
-              tma_prefetch_2d(&tm_h, nb * 64, ((ps.b * prm.nc + ps.c) * H + ps.h_begin) * 64);
           }
         }
         u += sg.nh;
@@ -488,16 +480,18 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   const uint64_t bdims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t bstr[2] = {uint64_t(p.G * p.N * 2), uint64_t(p.L * p.G * p.N * 2)};
   const uint32_t box3[3] = {64, 128, 1};
-  const uint64_t hdims[2] = {uint64_t(p.N), uint64_t(p.b * p.nc * p.H * p.P)};
-  const uint64_t hstr[1] = {uint64_t(p.N * 2)};
-  const uint32_t hbox[2] = {64, 64};
+  // hprev (rows p of each (b, c, h), N columns) as (64 columns, rows, N / 64 column halves), so
+  // that one box {64, 64, N / 64} lands as N / 64 swizzled 8 KB tiles
+  const uint64_t hdims[3] = {64, uint64_t(p.b * p.nc * p.H * p.P), uint64_t(p.N / 64)};
+  const uint64_t hstr[2] = {uint64_t(p.N * 2), 128};
+  const uint32_t hbox[3] = {64, 64, uint32_t(p.N / 64)};
   if (!encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, bdims, bstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, bdims, bstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
-      !encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hprev, hdims, hstr, hbox,
+      !encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, hprev, hdims, hstr, hbox,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why))
