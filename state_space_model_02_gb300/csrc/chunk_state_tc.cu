@@ -122,11 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t full = bar_full + 8 * s;
     const int t0 = c * Q + kb * 64;
     mbar_arrive_expect_tx(full, SM::kStage);
-    tma_load_3d(st, &tm_x, full, h0 * 64, t0, b);
-    tma_load_3d(st + kBox, &tm_x, full, (h0 + 1) * 64, t0, b);
-#pragma unroll
-    for (int j = 0; j < NT / 64; ++j)
-      tma_load_3d(st + SM::kX + j * kBox, &tm_B, full, g * prm.N + nt * NT + j * 64, t0, b);
+    // one box each: both heads' x tiles, and all NT / 64 column tiles of B
+    tma_load_4d(st, &tm_x, full, 0, t0, h0, b);
+    tma_load_4d(st + SM::kX, &tm_B, full, 0, t0, (g * prm.N + nt * NT) / 64, b);
     issued = kb + 1;
   };
 
@@ -255,19 +253,23 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
                                   const char** why) {
   const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
   CUtensorMap tx, tb, ts;
+  // TMA boxes cost about the same for 8 and 16 KB, so each k-block takes one box for x and one
+  // for B: x (b, L, H, P) viewed as (p, token, head, batch) with a box of two heads, and B
+  // (b, L, G, N) as (64 columns, token, N / 64 column blocks, batch) with a box of NT / 64 blocks;
+  // both land as 64-row x 128-byte swizzled tiles, one after the other.
   {
-    const uint64_t dims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
-    const uint64_t strides[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
-    const uint32_t box[3] = {64, 64, 1};
-    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box,
+    const uint64_t dims[4] = {64, uint64_t(p.L), uint64_t(p.H), uint64_t(p.b)};
+    const uint64_t strides[3] = {uint64_t(p.H * p.P * 2), uint64_t(p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
+    const uint32_t box[4] = {64, 64, 2, 1};
+    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
-    const uint64_t strides[2] = {uint64_t(p.G * p.N * 2), uint64_t(p.L * p.G * p.N * 2)};
-    const uint32_t box[3] = {64, 64, 1};
-    if (!encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, dims, strides, box,
+    const uint64_t dims[4] = {64, uint64_t(p.L), uint64_t(p.G * p.N / 64), uint64_t(p.b)};
+    const uint64_t strides[3] = {uint64_t(p.G * p.N * 2), 128, uint64_t(p.L * p.G * p.N * 2)};
+    const uint32_t box[4] = {64, 64, uint32_t(NT / 64), 1};
+    if (!encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, B, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }

@@ -165,7 +165,11 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
     if (why) *why = "cuTensorMapEncodeTiled is not available";
     return false;
   }
-  cuuint32_t estr[3] = {1, 1, 1};
+  if (rank < 1 || rank > 5) {
+    if (why) *why = "tensor map rank out of range";
+    return false;
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r =
       fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
          reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
