@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
   __shared__ float tile[kHeadsPerCta][ROW];
   const int64_t c = blockIdx.x, b = blockIdx.y, h0 = int64_t(blockIdx.z) * kHeadsPerCta;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_wait();    // cs2 / dtT may still be read by the previous step's kernels
+  grid_dep_launch();
 
   // all loads of the tile are issued before any is consumed (Q/32 per thread in flight)
   constexpr int kPer = Q * kHeadsPerCta / 256;
@@ -81,18 +83,14 @@ cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* 
                   static_cast<unsigned>((p.H + kHeadsPerCta - 1) / kHeadsPerCta));
   switch (p.Q) {
     case 64:
-      chunk_cumsum_kernel<64><<<grid, 256, 0, st>>>(dt, A, cs2, dtT, p.L, p.H, p.nc);
-      break;
+      return launch_pdl(chunk_cumsum_kernel<64>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
     case 128:
-      chunk_cumsum_kernel<128><<<grid, 256, 0, st>>>(dt, A, cs2, dtT, p.L, p.H, p.nc);
-      break;
+      return launch_pdl(chunk_cumsum_kernel<128>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
     case 256:
-      chunk_cumsum_kernel<256><<<grid, 256, 0, st>>>(dt, A, cs2, dtT, p.L, p.H, p.nc);
-      break;
+      return launch_pdl(chunk_cumsum_kernel<256>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace ssd

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
+  grid_dep_wait();  // hprev, cs2 and dtT come from the previous kernels
 
   const int64_t u_begin = unit_at_weight(prm.total_weight * blockIdx.x / gridDim.x, H, MT);
   const int64_t u_end = unit_at_weight(prm.total_weight * (blockIdx.x + 1) / gridDim.x, H, MT);
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (store_thread) bulk_wait_read0();  // the stores have read the staging buffer
   }
 
+  grid_dep_launch();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -458,8 +460,8 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
   auto kern = chunk_scan_tc_kernel<NB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, SM::kAlloc, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, st, maps[0], maps[1], maps[2], maps[3],
+                    maps[4], prm);
 }
 
 }  // namespace

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), NT);
     tmem_relinquish();
   }
+  grid_dep_wait();  // cs2 / dtT come from the previous kernel; S may still be read by older ones
   // decay weights of the (up to) two heads: w[k][t] = 2^(cs2_last - cs2_t) * dt_t
   for (int e = tid; e < 2 * Q; e += kThreads) {
     const int k = e / Q, t = e % Q;
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  grid_dep_launch();
   // teardown: drain whatever is still in flight, then release tensor memory
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb)
@@ -236,8 +238,7 @@ cudaError_t launch_nt(const Problem& p, const CUtensorMap& tx, const CUtensorMap
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.G * prm.pairs_per_group * prm.n_tiles),
                   static_cast<unsigned>(p.nc), static_cast<unsigned>(p.b));
-  kern<<<grid, kThreads, SM::kAlloc, st>>>(tx, tb, ts, prm);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), SM::kAlloc, st, tx, tb, ts, prm);
 }
 
 }  // namespace

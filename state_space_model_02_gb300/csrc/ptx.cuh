@@ -20,6 +20,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch (PDL)
+
+// Waits until the grids this one depends on have completed and their writes are visible.  A
+// kernel launched with programmatic stream serialization may start while its predecessor in the
+// stream is still running; it calls this before touching global memory.  No-op otherwise.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid in the stream start launching (its CTAs then wait in grid_dep_wait).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

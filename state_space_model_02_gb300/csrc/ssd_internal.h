@@ -37,6 +37,26 @@ inline Layout make_layout(const Problem& p) {
   return l;
 }
 
+// Launches `kern` on `st` with programmatic stream serialization: the kernel may begin (its
+// prologue: barrier init, tensor-memory allocation, tensor-map prefetch) while the previous
+// kernel in the stream is finishing, and waits in grid_dep_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Default limit of one bounded on-chip wait (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

@@ -44,7 +44,11 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
     HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
     int64_t Q, int64_t total4) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= total4) return;
+  grid_dep_wait();  // S and cs2 come from the previous kernels
+  if (idx >= total4) {
+    grid_dep_launch();
+    return;
+  }
   const int64_t per_bh = PN / 4;
   const int64_t bh = idx / per_bh, e = (idx % per_bh) * 4;
   const int64_t bi = bh / H, h = bh % H;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
     }
   }
   if (final_state) *reinterpret_cast<float4*>(final_state + bh * PN + e) = hv;
+  grid_dep_launch();
 }
 
 __device__ __forceinline__ void store1(float* dst, float v) { *dst = v; }
@@ -104,7 +109,11 @@ __global__ void __launch_bounds__(256) state_passing_scalar_kernel(
     HT* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN, int64_t nc,
     int64_t Q, int64_t total) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= total) return;
+  grid_dep_wait();
+  if (idx >= total) {
+    grid_dep_launch();
+    return;
+  }
   const int64_t bh = idx / PN, e = idx % PN;
   const int64_t bi = bh / H, h = bh % H;
   const int64_t cstride = H * PN;
@@ -117,6 +126,7 @@ __global__ void __launch_bounds__(256) state_passing_scalar_kernel(
     hv = fmaf(ex2(__ldg(dec + c * Q)), hv, load1(Sp + c * cstride));
   }
   if (final_state) final_state[bh * PN + e] = hv;
+  grid_dep_launch();
 }
 
 }  // namespace
@@ -130,18 +140,18 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
   if (vec) {
     if (p.io_bf16)
-      state_passing_vec4_kernel<uint16_t><<<blocks, 256, 0, st>>>(
-          static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+      return launch_pdl(state_passing_vec4_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
+                        init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
-      state_passing_vec4_kernel<float><<<blocks, 256, 0, st>>>(
-          static_cast<const float*>(S), cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+      return launch_pdl(state_passing_vec4_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
+                        init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   } else {
     if (p.io_bf16)
-      state_passing_scalar_kernel<uint16_t><<<blocks, 256, 0, st>>>(
-          static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+      return launch_pdl(state_passing_scalar_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
+                        init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
-      state_passing_scalar_kernel<float><<<blocks, 256, 0, st>>>(
-          static_cast<const float*>(S), cs2, init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
+      return launch_pdl(state_passing_scalar_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
+                        init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   }
   return cudaGetLastError();
 }
