@@ -10,9 +10,9 @@
 // chunk_cumsum row; zero padding past the sequence end leaves it unchanged).
 //
 // The loop over chunks is a dependent FMA chain per element, so the kernel is bound by HBM
-// latency x bandwidth: each thread owns 4 consecutive state elements (4 values of S per
-// chunk, stored in the I/O dtype) and keeps kDepth chunks of S in flight in registers ahead of
-// the chain.  The chain itself runs in float32.
+// latency x bandwidth: each thread owns consecutive state elements -- 8 (one 16-byte load of S
+// per chunk) when S is bf16, 4 when it is float32 -- and keeps kDepth chunks of S in flight in
+// registers ahead of the chain.  The chain itself runs in float32.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -36,6 +36,82 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
   u.x = pack_bf16x2(v.x, v.y);
   u.y = pack_bf16x2(v.z, v.w);
   *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// bf16 S / hprev, 8 elements per thread.
+__global__ void __launch_bounds__(256, 4) state_passing_bf16x8_kernel(
+    const uint16_t* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
+    uint16_t* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN,
+    int64_t nc, int64_t Q, int64_t total8) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  grid_dep_wait();  // S and cs2 come from the previous kernels
+  if (idx >= total8) {
+    grid_dep_launch();
+    return;
+  }
+  const int64_t per_bh = PN / 8;
+  const int64_t bh = idx / per_bh, e = (idx % per_bh) * 8;
+  const int64_t bi = bh / H, h = bh % H;
+  const int64_t cstride = H * PN;  // elements between chunks in S / hprev
+  uint16_t* Hp = hprev + (bi * nc * H + h) * PN + e;
+  const int n = static_cast<int>(nc);
+
+  float hv[8];
+  if (init) {
+    const float4 a0 = __ldg(reinterpret_cast<const float4*>(init + bh * PN + e));
+    const float4 a1 = __ldg(reinterpret_cast<const float4*>(init + bh * PN + e + 4));
+    hv[0] = a0.x; hv[1] = a0.y; hv[2] = a0.z; hv[3] = a0.w;
+    hv[4] = a1.x; hv[5] = a1.y; hv[6] = a1.z; hv[7] = a1.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hv[i] = 0.f;
+  }
+  uint4 sbuf[kDepth];
+  float dbuf[kDepth];
+  const uint16_t* sp = S + (bi * nc * H + h) * PN + e;
+  const float* dp = cs2 + bh * nc * Q + (Q - 1);
+#pragma unroll
+  for (int k = 0; k < kDepth; ++k) {
+    if (k < n) {
+      sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
+      dbuf[k] = __ldg(dp);
+      sp += cstride;
+      dp += Q;
+    }
+  }
+  for (int c0 = 0; c0 < n; c0 += kDepth) {
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) {
+      const int c = c0 + k;
+      if (c < n) {
+        uint4 o;
+        o.x = pack_bf16x2(hv[0], hv[1]);
+        o.y = pack_bf16x2(hv[2], hv[3]);
+        o.z = pack_bf16x2(hv[4], hv[5]);
+        o.w = pack_bf16x2(hv[6], hv[7]);
+        *reinterpret_cast<uint4*>(Hp) = o;
+        Hp += cstride;
+        const float d = ex2(dbuf[k]);
+        const uint32_t w[4] = {sbuf[k].x, sbuf[k].y, sbuf[k].z, sbuf[k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          hv[2 * i] = fmaf(d, hv[2 * i], bf16lo_to_f32(w[i]));
+          hv[2 * i + 1] = fmaf(d, hv[2 * i + 1], bf16hi_to_f32(w[i]));
+        }
+        if (c + kDepth < n) {  // refill this ring entry with chunk c + kDepth
+          sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
+          dbuf[k] = __ldg(dp);
+          sp += cstride;
+          dp += Q;
+        }
+      }
+    }
+  }
+  if (final_state) {
+    *reinterpret_cast<float4*>(final_state + bh * PN + e) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<float4*>(final_state + bh * PN + e + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+  }
+  grid_dep_launch();
 }
 
 template <typename HT>
@@ -135,6 +211,13 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
                                  const float* init, void* hprev, float* final_state,
                                  cudaStream_t st) {
   const int64_t PN = p.P * p.N;
+  if (p.io_bf16 && PN % 8 == 0) {
+    const int64_t total8 = p.b * p.H * (PN / 8);
+    const unsigned blocks8 = static_cast<unsigned>((total8 + 255) / 256);
+    return launch_pdl(state_passing_bf16x8_kernel, dim3(blocks8), dim3(256), 0, st,
+                      static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev),
+                      final_state, p.H, PN, p.nc, p.Q, total8);
+  }
   const bool vec = (PN % 4) == 0;
   const int64_t total = p.b * p.H * (vec ? PN / 4 : PN);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
