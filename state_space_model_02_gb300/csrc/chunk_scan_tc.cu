@@ -165,7 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
-  grid_dep_wait();  // hprev, cs2 and dtT come from the previous kernels
+  // hprev, cs2 and dtT come from the previous kernels: the producer and the epilogue (the roles
+  // that read them from global memory) wait for those in grid_dep_wait; the other roles only
+  // see data through the producer's barriers
 
   const int64_t u_begin = unit_at_weight(prm.total_weight * blockIdx.x / gridDim.x, H, MT);
   const int64_t u_end = unit_at_weight(prm.total_weight * (blockIdx.x + 1) / gridDim.x, H, MT);
@@ -176,20 +178,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gi = 0, si = 0;
       bool pend_cb = false, pend_hp[2] = {false, false}, pend_xs[2] = {false, false};
       uint32_t ph_cb = 0, ph_hp[2] = {0, 0}, ph_xs[2] = {0, 0};
+      auto load_cb = [&](const Segment& sg) {
+        const int i0 = sg.mt * 128, jrows = i0 + 128;
+        mbar_arrive_expect_tx(bar(kCbFull), NB * kBox128 + NB * jrows * 128);
+        for (int nb = 0; nb < NB; ++nb)
+          tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + nb * 64,
+                      sg.c * Q + i0, sg.b);
+        for (int nb = 0; nb < NB; ++nb)
+          for (int jb = 0; jb < jrows / 128; ++jb)
+            tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar(kCbFull),
+                        sg.g * N + nb * 64, sg.c * Q + jb * 128, sg.b);
+      };
+      // x slot s of a head: its x box(es) now, its cs2 / dt rows (from the previous kernel) later;
+      // the slot's barrier expects all three from the start
+      auto load_x = [&](const Segment& sg, int hh, uint32_t s) {
+        const int jrows = sg.mt * 128 + 128;
+        const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
+        const uint32_t xb = bar(kXsFull0 + s);
+        mbar_arrive_expect_tx(xb, jrows * 128 + 2 * jrows * 4);
+        for (int jb = 0; jb < jrows / 128; ++jb)
+          tma_load_3d(xs + SM::kXsX + jb * kBox128, &tm_x, xb, hh * 64, sg.c * Q + jb * 128, sg.b);
+      };
+      // C, B and x are inputs of the step, not written by the kernels before this one (and every
+      // kernel before the previous one has completed): the first segment's C and B and the first
+      // two heads' x are requested before waiting for the previous kernels
+      int pre_x = 0;
+      if (u_begin < u_end) {
+        const Segment sg0 = segment_at(u_begin, u_end, prm);
+        load_cb(sg0);
+        pend_cb = true;
+        pre_x = sg0.nh < 2 ? sg0.nh : 2;
+        for (int hi = 0; hi < pre_x; ++hi) load_x(sg0, sg0.h_begin + hi, uint32_t(hi));
+      }
+      grid_dep_wait();
       for (int64_t u = u_begin; u < u_end; ++si) {
         const Segment sg = segment_at(u, u_end, prm);
         const int i0 = sg.mt * 128, jrows = i0 + 128;
         // C and B of the new segment overwrite regions the previous segment's MMAs read
         if (si >= 1) (void)mbar_wait(bar(kSegFree), (si - 1) & 1, ctl);
-        if (!*abort_flag) {
-          mbar_arrive_expect_tx(bar(kCbFull), NB * kBox128 + NB * jrows * 128);
-          for (int nb = 0; nb < NB; ++nb)
-            tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + nb * 64,
-                        sg.c * Q + i0, sg.b);
-          for (int nb = 0; nb < NB; ++nb)
-            for (int jb = 0; jb < jrows / 128; ++jb)
-              tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar(kCbFull),
-                          sg.g * N + nb * 64, sg.c * Q + jb * 128, sg.b);
+        if (si >= 1 && !*abort_flag) {
+          load_cb(sg);
           pend_cb = true;
           ph_cb = si & 1;
         }
@@ -208,12 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ph_hp[s] = use & 1;
           }
           if (gi >= 2) (void)mbar_wait(bar(kXsEmpty0 + s), (use - 1) & 1, ctl);
-          if (!*abort_flag) {
+          if (!*abort_flag || gi < uint32_t(pre_x)) {
+            // (a slot whose x went out early must still get its cs2 / dt bytes)
             const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
             const uint32_t xb = bar(kXsFull0 + s);
-            mbar_arrive_expect_tx(xb, jrows * 128 + 2 * jrows * 4);
-            for (int jb = 0; jb < jrows / 128; ++jb)
-              tma_load_3d(xs + SM::kXsX + jb * kBox128, &tm_x, xb, hh * 64, sg.c * Q + jb * 128, sg.b);
+            if (gi >= uint32_t(pre_x)) load_x(sg, hh, s);
             const int64_t crow = ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q;
             bulk_load(xs + SM::kXsCs, prm.cs2 + crow, jrows * 4, xb);
             bulk_load(xs + SM::kXsDt, prm.dtT + crow, jrows * 4, xb);
@@ -392,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
     const bool store_thread = warp == 2 + kMaskWarps && lane == 0;
     uint32_t gi = 0;
+    grid_dep_wait();  // cs2 comes from the previous kernels
     for (int64_t u = u_begin; u < u_end;) {
       const Segment sg = segment_at(u, u_end, prm);
       const int i0 = sg.mt * 128, row = i0 + r;

@@ -97,6 +97,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), NT);
     tmem_relinquish();
   }
+  // thread-0 bookkeeping of loads in flight (for the drain on abort)
+  int issued = 0, consumed = 0;
+  auto issue = [&](int kb) {
+    const int s = kb & 1;
+    const uint32_t st = sb + s * SM::kStage;
+    const uint32_t full = bar_full + 8 * s;
+    const int t0 = c * Q + kb * 64;
+    mbar_arrive_expect_tx(full, SM::kStage);
+    // one box each: both heads' x tiles, and all NT / 64 column tiles of B
+    tma_load_4d(st, &tm_x, full, 0, t0, h0, b);
+    tma_load_4d(st + SM::kX, &tm_B, full, 0, t0, (g * prm.N + nt * NT) / 64, b);
+    issued = kb + 1;
+  };
+
+  // x and B are inputs of the step, not written by the kernels before this one (and every kernel
+  // before the previous one has completed), so the first two k-blocks are requested before
+  // waiting for the previous kernel's cs2 / dtT
+  if (tid == 0) {
+    issue(0);
+    if (kblocks > 1) issue(1);
+  }
   grid_dep_wait();  // cs2 / dtT come from the previous kernel; S may still be read by older ones
   // decay weights of the (up to) two heads: w[k][t] = 2^(cs2_last - cs2_t) * dt_t
   for (int e = tid; e < 2 * Q; e += kThreads) {
@@ -115,24 +136,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, NT, 1, 1);
 
-  // thread-0 bookkeeping of loads in flight (for the drain on abort)
-  int issued = 0, consumed = 0;
-  auto issue = [&](int kb) {
-    const int s = kb & 1;
-    const uint32_t st = sb + s * SM::kStage;
-    const uint32_t full = bar_full + 8 * s;
-    const int t0 = c * Q + kb * 64;
-    mbar_arrive_expect_tx(full, SM::kStage);
-    // one box each: both heads' x tiles, and all NT / 64 column tiles of B
-    tma_load_4d(st, &tm_x, full, 0, t0, h0, b);
-    tma_load_4d(st + SM::kX, &tm_B, full, 0, t0, (g * prm.N + nt * NT) / 64, b);
-    issued = kb + 1;
-  };
-
-  if (tid == 0) {
-    issue(0);
-    if (kblocks > 1) issue(1);
-  }
   for (int kb = 0; kb < kblocks; ++kb) {
     const int s = kb & 1;
     const uint32_t ph = (kb >> 1) & 1;
