@@ -175,6 +175,25 @@ ssd_status ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const float* d
                            const void* B, const void* C, const float* D, const float* init_state,
                            void* y, float* final_state, void* stream);
 
+/*
+ * Recurrent form over a short run of tokens -- the decoding step ("Compiler-First State Space
+ * Duality and Portable O(1) Autoregressive Caching for Inference", technical summary section 2:
+ * the fixed-size state is the cache, updated on the device token after token with no host
+ * round trip per token).  For every (batch, head), in place, over shape->seqlen tokens t:
+ *     state <- exp(dt_t * A_h) * state + dt_t * outer(x_t, B_t),    y_t = state @ C_t + D_h * x_t
+ *   - x, y (batch, seqlen, nheads, headdim), dt (batch, seqlen, nheads), B, C (batch, seqlen,
+ *     ngroups, dstate), A, D (nheads): as for ssd_fwd (D may be null).
+ *   - state: float32 (batch, nheads, headdim, dstate), read at the start and overwritten with the
+ *     state after the last token; it must not alias any input.
+ *   - shape->chunk and shape->flags are ignored.  One launch reads and writes the state once,
+ *     whatever seqlen is; the recurrence runs in float32.
+ *   - Needs no workspace.  SSD_ERR_UNSUPPORTED unless dstate is a multiple of 64 with
+ *     dstate / 64 <= 32, and headdim * dstate / 64 is a multiple of 32 and at most 512.
+ */
+ssd_status ssd_decode(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                      const void* B, const void* C, const float* D, float* state, void* y,
+                      void* stream);
+
 /* Static description of a status code. */
 const char* ssd_status_str(ssd_status status);
 

@@ -336,6 +336,29 @@ ssd_status ssd_selftest_wait_timeout(uint32_t* status_word, uint64_t timeout_ns,
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "selftest launch");
 }
 
+ssd_status ssd_decode(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                      const void* B, const void* C, const float* D, float* state, void* y,
+                      void* stream) {
+  if (!shape) return fail(SSD_ERR_INVALID, "shape is null");
+  ssd_shape s = *shape;
+  s.chunk = 64;  // the recurrent form has no chunks
+  ssd::Problem p;
+  SSD_TRY(make_problem(&s, &p));
+  SSD_TRY(need(x, "x"));
+  SSD_TRY(need(dt, "dt"));
+  SSD_TRY(need(A, "A"));
+  SSD_TRY(need(B, "B"));
+  SSD_TRY(need(C, "C"));
+  SSD_TRY(need(state, "state"));
+  SSD_TRY(need(y, "y"));
+  SSD_TRY(maybe(D, "D"));
+  if (!ssd::decode_ok(p)) return fail(SSD_ERR_UNSUPPORTED, "decode: unsupported headdim / dstate");
+  const cudaError_t e = ssd::launch_decode(p, x, dt, A, B, C, D, state, y, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  g_last_error[0] = '\0';
+  return SSD_OK;
+}
+
 const char* ssd_status_str(ssd_status s) {
   switch (s) {
     case SSD_OK: return "ok";

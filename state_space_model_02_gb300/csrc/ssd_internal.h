@@ -76,6 +76,12 @@ cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* 
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st);
 
+// Recurrent form over a short run of tokens (decoding); applicability by decode_ok.
+bool decode_ok(const Problem& p);
+cudaError_t launch_decode(const Problem& p, const void* x, const float* dt, const float* A,
+                          const void* B, const void* C, const float* D, float* state, void* y,
+                          cudaStream_t st);
+
 // Tensor-core (tcgen05) kernels.  Applicability is decided by the *_tc_ok predicates.
 bool chunk_state_tc_ok(const Problem& p);
 bool chunk_scan_tc_ok(const Problem& p);

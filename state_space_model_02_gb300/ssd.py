@@ -19,8 +19,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_E
 # Every entry point of include/ssd.h, in declaration order.
 EXPORTS = ("ssd_workspace_bytes", "ssd_get_workspace_layout", "ssd_fwd", "ssd_chunk_cumsum",
            "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_read_status",
-           "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_status_str", "ssd_last_error",
-           "ssd_kernel_plan")
+           "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_decode", "ssd_status_str",
+           "ssd_last_error", "ssd_kernel_plan")
 
 
 class Shape(ctypes.Structure):
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH):
         "ssd_read_status": ([vp, vp], ctypes.c_int),
         "ssd_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ctypes.c_int),
         "ssd_fwd_noalloc": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ssd_decode": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "ssd_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "ssd_last_error": ([], ctypes.c_char_p),
         "ssd_kernel_plan": ([sp], ctypes.c_int),
@@ -193,6 +194,29 @@ def fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None, final_sta
                                 workspace.numel(), _stream(stream))
     _check(rc)
     return y, final_state
+
+
+def decode(x, dt, A, B, C, D, state, *, y=None, stream=None):
+    """ssd_decode: advances ``state`` (fp32, (b,H,P,N), updated in place) over the L tokens of
+    x (b,L,H,P) and returns y (b,L,H,P).  B, C (b,L,G,N) in x's dtype; dt (b,L,H), A and D (H)
+    in fp32.  Work is enqueued on ``stream`` (default: current).
+    """
+    torch = _torch()
+    prob = problem_of(x, B, 64)
+    b, L, H, P, N, G = prob.batch, prob.seqlen, prob.nheads, prob.headdim, prob.dstate, prob.ngroups
+    _need(x, "x", x.dtype)
+    _need(B, "B", x.dtype, (b, L, G, N))
+    _need(C, "C", x.dtype, (b, L, G, N))
+    _need(dt, "dt", torch.float32, (b, L, H))
+    _need(A, "A", torch.float32, (H,))
+    _need(D, "D", torch.float32, (H,))
+    _need(state, "state", torch.float32, (b, H, P, N))
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", x.dtype, x.shape)
+    _check(load_library().ssd_decode(ctypes.byref(prob.c_shape()), _p(x), _p(dt), _p(A), _p(B), _p(C),
+                                      _p(D), _p(state), _p(y), _stream(stream)))
+    return y
 
 
 def chunk_cumsum(prob, dt, A, workspace, stream=None):

@@ -116,3 +116,23 @@ def test_selftest_rejects_bad_limits(lib):
     assert lib.ssd_selftest_wait_timeout(None, 1000, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(0x1000), 2_000_000_000, None) == 1
+
+
+def test_decode_rejects_bad_arguments_before_any_launch(lib):
+    good = ctypes.c_void_p(0x100000)
+    args = [good] * 8
+    s = shape(seqlen=1).c_shape()
+    # dstate not a multiple of 64
+    bad = shape(seqlen=1, dstate=48).c_shape()
+    assert lib.ssd_decode(ctypes.byref(bad), *args, None) == 2
+    # null state
+    a = list(args)
+    a[6] = None
+    assert lib.ssd_decode(ctypes.byref(s), *a, None) == 1
+    # misaligned x
+    a = list(args)
+    a[0] = ctypes.c_void_p(0x100004)
+    assert lib.ssd_decode(ctypes.byref(s), *a, None) == 3
+    # the chunk field is not used by the recurrent form
+    odd = shape(seqlen=1, chunk=100).c_shape()
+    assert lib.ssd_decode(ctypes.byref(odd), *([None] * 8), None) == 1  # null x, not the chunk
