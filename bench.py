@@ -9,6 +9,10 @@ time comes from CUDA events around the four launches, issued back to back as ssd
 per-kernel times (for the roofline) from a second pass with an event between the launches.
 ``--impl reference`` times the float64 CPU oracle instead, on a bounded sample of the same
 workload.  Rank 0 prints one JSON line.
+
+Workloads named ``decode_*`` time the recurrent form instead (ssd_decode): one step is one
+launch that advances the resident float32 state of every (batch, head) by ``seqlen`` tokens;
+the metric is decoded tokens/s and the roofline is HBM (the state is read and written once).
 """
 import argparse
 import hashlib
@@ -27,6 +31,15 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "mamba2_130m_layer"
 METRIC = "SSD forward tokens/s on 1 GB300 + per-kernel % of HBM/tensor roofline"
+METRIC_DECODE = "SSD decode tokens/s on 1 GB300 + % of HBM roofline"
+
+
+def is_decode(workload):
+    return workload.startswith("decode")
+
+
+def metric_of(workload):
+    return METRIC_DECODE if is_decode(workload) else METRIC
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
 
 
@@ -86,7 +99,8 @@ def load_peaks():
 
 def source_digest(kernel):
     files = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state_tc.cu",
-             "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu"}
+             "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu",
+             "decode": "decode.cu"}
     p = os.path.join(ROOT, "state_space_model_02_gb300", "csrc", files[kernel])
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -167,6 +181,16 @@ class ClockSampler:
 # ------------------------------------------------------------------------- CPU baseline
 
 
+def algorithmic_decode(shape):
+    """Minimum HBM bytes and FLOPs of one decode launch: the state read and written once
+    (float32), each token's x, dt, B, C read and y written once, A and D read once."""
+    b, T, H, P, N, G = (shape[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    e = 2 if shape["io_dtype"] == "bf16" else 4
+    by = 2 * b * H * P * N * 4 + b * T * (2 * H * P * e + 2 * G * N * e + H * 4) + 2 * H * 4
+    fl = b * T * H * P * (4 * N + 2)   # update (2 per element) + C contraction (2) + D x
+    return by, fl
+
+
 def cpu_baseline(inp, budget_s):
     """The float64 oracle as it stands, on the host cores, over a bounded sample of the
     workload: whole (batch, head) sequences, as many as fit the time budget."""
@@ -225,7 +249,7 @@ def run_reference(args):
         vals.append(base["value"])
     v = float(np.median(vals))
     tokens = shape["batch"] * shape["seqlen"]
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_of(args.workload), "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tokens / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload, **shape},
@@ -263,6 +287,8 @@ def run_ours(args):
                 C=io(inp.C), D=torch.from_numpy(inp.D),
                 init=None if inp.init is None else torch.from_numpy(inp.init))
     d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    if is_decode(args.workload):
+        return run_decode(args, torch, dist, ssd, ws, rank, local, dev, shape, inp, host, d)
     prob = ssd.problem_of(d["x"], d["B"], inp.chunk)
     wsbuf = ssd.alloc_workspace(prob, dev)
     y = torch.empty_like(d["x"])
@@ -417,6 +443,118 @@ def run_ours(args):
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in kern[n].items()}
                     for n in KERNELS},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": len(KERNELS) * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_decode(args, torch, dist, ssd, ws, rank, local, dev, shape, inp, host, d):
+    """The decode arm: one ssd_decode launch per step over resident state and inputs."""
+    b, T, H, P, N = (shape[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
+    state = (d["init"].clone() if d["init"] is not None
+             else torch.zeros((b, H, P, N), dtype=torch.float32, device=dev))
+    y = torch.empty_like(d["x"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(k):
+        flush.fill_(k & 0xFF)
+        flush_rd.max()
+
+    def step():
+        ssd.decode(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], state, y=y, stream=stream)
+
+    for k in range(max(3, args.warmup)):
+        flush_l2(k)
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush_l2(k)
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = b * T
+    value = ws * tokens / (ms_step * 1e-3)
+    by, fl = algorithmic_decode(shape)
+    peaks = load_peaks()
+    ach = by / (ms_step * 1e-3) / 1e9
+    roofline = {"kernel": "decode", "bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": ach / peaks["hbm"], "traffic": profiled_traffic("decode", args.workload),
+                "peak_source": peaks["src"] + " (MEASURED_PEAKS.json burst)"
+                if peaks["src"] == "measured" else "fallback"}
+
+    # end to end: the step's token inputs (x, dt, B, C) from pinned host memory, y back to pinned
+    # host memory; the state stays resident on the device (it is the cache being decoded from)
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: host[k].pin_memory() for k in ("x", "dt", "B", "C")}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            for k, v in pin.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            yy = ssd.decode(dev_in["x"], dev_in["dt"], d["A"], dev_in["B"], dev_in["C"], d["D"], state,
+                            y=y, stream=stream)
+            y_host.copy_(yy, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "note": "state resident on the device across steps"}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+    line = {
+        "metric": METRIC_DECODE, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if inp.io_dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": args.workload, **shape,
+                   "l2": "flushed before every step (256 MiB write + 256 MiB read, outside the timed events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "state": "float32 (b, H, P, N), read and written once per step"},
+        "roofline": roofline,
+        "kernels": {"decode": {"us": 1e3 * ms_step, "share": 1.0, "alg_bytes": by, "alg_flops": fl}},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -37,6 +37,12 @@ CONFIGS = {
                              chunk=256, io_dtype="bf16", init=False),
     "long_256k": dict(batch=1, seqlen=262144, nheads=32, headdim=64, dstate=128, ngroups=1,
                       chunk=256, io_dtype="bf16", init=False),
+    # decoding (the recurrent form): seqlen is the number of tokens one launch advances the
+    # state by; the state (b, H, P, N) float32 is the whole per-sequence cache
+    "decode_2p7b_b64_t1": dict(batch=64, seqlen=1, nheads=80, headdim=64, dstate=128, ngroups=1,
+                               chunk=64, io_dtype="bf16", init=True),
+    "decode_2p7b_b64_t16": dict(batch=64, seqlen=16, nheads=80, headdim=64, dstate=128, ngroups=1,
+                                chunk=64, io_dtype="bf16", init=True),
 }
 
 

@@ -125,6 +125,9 @@ def test_decode_rejects_bad_arguments_before_any_launch(lib):
     # dstate not a multiple of 64
     bad = shape(seqlen=1, dstate=48).c_shape()
     assert lib.ssd_decode(ctypes.byref(bad), *args, None) == 2
+    # dstate / 64 not a power of two
+    bad = shape(seqlen=1, dstate=192).c_shape()
+    assert lib.ssd_decode(ctypes.byref(bad), *args, None) == 2
     # null state
     a = list(args)
     a[6] = None

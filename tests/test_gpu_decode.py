@@ -48,7 +48,7 @@ def oracle(inp):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("T", [1, 3, 16])
+@pytest.mark.parametrize("T", [1, 3, 7, 16])
 @pytest.mark.parametrize("N", [64, 128, 256])
 def test_decode_matches_oracle(dtype, T, N):
     inp = synth.make_inputs(batch=3, seqlen=T, nheads=5, headdim=64, dstate=N, io_dtype=dtype,
@@ -71,6 +71,28 @@ def test_decode_groups_no_D_zero_state():
 def test_decode_state_size_512():
     inp = synth.make_inputs(batch=1, seqlen=2, nheads=3, headdim=64, dstate=512, io_dtype="bf16",
                             init=True, seed=33)
+    y, st = run_decode(inp)
+    y_ref, st_ref = oracle(inp)
+    assert rel(y, y_ref) <= Y_TOL["bf16"]
+    assert rel(st, st_ref) <= STATE_TOL
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_state_size_1024_per_head_kernel(dtype):
+    # N = 1024 is beyond the row-streaming kernel's sizes: the per-head kernel serves it
+    inp = synth.make_inputs(batch=2, seqlen=5, nheads=3, headdim=16, dstate=1024, io_dtype=dtype,
+                            init=True, seed=35)
+    y, st = run_decode(inp)
+    y_ref, st_ref = oracle(inp)
+    assert rel(y, y_ref) <= Y_TOL[dtype]
+    assert rel(st, st_ref) <= STATE_TOL
+
+
+def test_decode_many_heads_partial_last_block():
+    # 1 x 3 heads x (16 x 128) floats = 6 warps of 1024 floats in the row-streaming kernel:
+    # the second block of four warps is half empty
+    inp = synth.make_inputs(batch=1, seqlen=9, nheads=3, headdim=16, dstate=128, io_dtype="bf16",
+                            init=True, seed=37)
     y, st = run_decode(inp)
     y_ref, st_ref = oracle(inp)
     assert rel(y, y_ref) <= Y_TOL["bf16"]
