@@ -17,8 +17,8 @@
 // column table; every factor stays inside float32 range (|cs2| over 32 tokens <= 32*max|dt A|/ln2).
 //
 // Persistent CTAs (one per SM: 512 TMEM columns, ~214 KB shared memory, 14 warps) walk a
-// contiguous range of (batch, chunk, m-tile, head) units, weighted by the m-tile's causal
-// width; CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).  Warp
+// contiguous range of (batch, chunk, m-tile, head) units, weighted 2 : 3 for the two m-tiles
+// of a 256-token chunk (their measured cost ratio); CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).  Warp
 // roles, synchronised through mbarriers so the kinds of work overlap across heads:
 //   warp 0      TMA producer: C and B per segment; per head hprev (2-slot ring, freed once Y2
 //               is done; one box) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are
@@ -89,14 +89,19 @@ enum : int {
   kYFull0 = kPEmpty0 + 4, kYFull1, kYEmpty0, kYEmpty1, kDrain
 };
 
-// First unit whose starting weight is >= w.  Units are ordered (b, c, m-tile, h); a unit of
-// m-tile mt has weight mt + 1 (its causal width in 128-column blocks).
+// Work weights of the two 128-row m-tiles of a 256-token chunk (the second one's causal
+// width is twice the first's, but its measured cost per head is about 1.5x, since loads and
+// handoffs, not the mask and MMA work, dominate a unit).
+constexpr int64_t kWeightMt0 = 2, kWeightMt1 = 3;
+
+// First unit whose starting weight is >= w.  Units are ordered (b, c, m-tile, h); with one
+// m-tile per chunk every unit weighs 1.
 __device__ __forceinline__ int64_t unit_at_weight(int64_t w, int32_t H, int32_t MT) {
   if (MT == 1) return w;
-  const int64_t wbc = 3 * int64_t(H);
+  const int64_t wbc = (kWeightMt0 + kWeightMt1) * H;
   const int64_t bc = w / wbc, rem = w % wbc;
-  if (rem < H) return bc * 2 * H + rem;
-  const int64_t h = (rem - H + 1) / 2;
+  if (rem <= kWeightMt0 * H) return bc * 2 * H + (rem + kWeightMt0 - 1) / kWeightMt0;
+  const int64_t h = (rem - kWeightMt0 * H + kWeightMt1 - 1) / kWeightMt1;
   return h >= H ? (bc + 1) * 2 * H : bc * 2 * H + H + h;
 }
 
@@ -535,7 +540,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.MT = static_cast<int32_t>(p.Q / 128);
   prm.units = p.b * p.nc * prm.MT * p.H;
-  prm.total_weight = p.b * p.nc * p.H * (prm.MT == 2 ? 3 : 1);
+  prm.total_weight = p.b * p.nc * p.H * (prm.MT == 2 ? kWeightMt0 + kWeightMt1 : 1);
   prm.cs2 = cs2;
   prm.dtT = dtT;
   prm.D = D;

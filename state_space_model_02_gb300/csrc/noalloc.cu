@@ -15,7 +15,7 @@
 // call should therefore come before any stream capture on that device.
 #include <mutex>
 
-#include "../../include/ssd.h"
+#include "ssd.h"
 #include "ssd_internal.h"
 
 namespace {

@@ -6,7 +6,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/ssd.h"
+#include "ssd.h"
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
