@@ -4,21 +4,21 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "ssd_ref.c")
+SRCS = [os.path.join(HERE, "ssd_ref.c"), os.path.join(HERE, "selective_ref.c")]
 LIB = os.path.join(HERE, "libssd_ref.so")
 
 
 def build(force: bool = False) -> str:
-    """Compile ssd_ref.c into libssd_ref.so next to it; returns the library path.
+    """Compile the oracle's C files into libssd_ref.so next to them; returns the library path.
 
     Plain -O2 with OpenMP; no -march/-ffast-math so results are the same on
     x86_64 and aarch64 hosts (IEEE double, no reassociation).
     """
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(map(os.path.getmtime, SRCS)):
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
-           "-std=c11", SRC, "-o", tmp, "-lm"]
+           "-std=c11", *SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -106,3 +106,66 @@ def make_config(name: str, seed: int = 0, **overrides) -> SSDInputs:
     cfg = dict(CONFIGS[name])
     cfg.update(overrides)
     return make_inputs(seed=seed, **cfg)
+
+
+# ---------------------------------------------------------------- Mamba-1 selective scan
+#
+# "3.3 Hardware-aware algorithm and GPU memory hierarchy", section 2.1: x and delta are
+# (batch, L, D) with D channels, B and C (batch, L, N), A one value per (channel, state).
+# Layer shapes of Mamba-1 130M / 2.8B (d_inner 1536 / 5120, state 16); section 5.1's
+# sequences of 8192 tokens and more.  Same distributions as above, drawn in the order
+# x, B, C, delta_raw, A_u, D, init:
+#   x, B, C ~ N(0, 1) in the I/O dtype; delta = clip(softplus(N(-3, 1)), 1e-3, 0.1) in the
+#   I/O dtype; A (D, N) = -exp(U(ln a_lo, ln a_hi)); Dskip ~ N(0, 1); init (b, D, N) ~ N(0, 0.1).
+
+SELECTIVE_CONFIGS = {
+    "mamba1_tiny_fp32": dict(batch=1, seqlen=256, dim=64, dstate=16, io_dtype="f32", init=False),
+    "mamba1_130m_layer": dict(batch=4, seqlen=2048, dim=1536, dstate=16, io_dtype="bf16", init=False),
+    "mamba1_2p8b_layer": dict(batch=2, seqlen=8192, dim=5120, dstate=16, io_dtype="bf16", init=True),
+}
+
+
+@dataclass
+class SelectiveInputs:
+    """Host arrays of one selective-scan problem.  x/delta/B/C: float32 or bf16 bits (uint16)."""
+    x: np.ndarray
+    delta: np.ndarray
+    A: np.ndarray
+    B: np.ndarray
+    C: np.ndarray
+    D: Optional[np.ndarray]
+    init: Optional[np.ndarray]
+    io_dtype: str
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def shape(self):
+        b, L, D = self.x.shape
+        return dict(batch=b, seqlen=L, dim=D, dstate=self.B.shape[2], io_dtype=self.io_dtype)
+
+
+def make_selective_inputs(batch, seqlen, dim, dstate, io_dtype="bf16", init=False, seed=0,
+                          a_range=(1.0, 16.0), with_D=True) -> SelectiveInputs:
+    if io_dtype not in ("bf16", "f32"):
+        raise ValueError("io_dtype must be 'bf16' or 'f32'")
+    rng = np.random.default_rng(seed)
+    b, L, D, N = batch, seqlen, dim, dstate
+    x = rng.standard_normal((b, L, D), dtype=np.float32)
+    Bm = rng.standard_normal((b, L, N), dtype=np.float32)
+    Cm = rng.standard_normal((b, L, N), dtype=np.float32)
+    d_raw = rng.normal(-3.0, 1.0, size=(b, L, D))
+    a_u = rng.uniform(np.log(a_range[0]), np.log(a_range[1]), size=(D, N))
+    Dskip = rng.standard_normal(D).astype(np.float32)
+    h0 = rng.normal(0.0, 0.1, size=(b, D, N)).astype(np.float32) if init else None
+    delta = np.clip(np.logaddexp(0.0, d_raw), 1e-3, 0.1).astype(np.float32)
+    A = (-np.exp(a_u)).astype(np.float32)
+    if io_dtype == "bf16":
+        x, Bm, Cm, delta = to_bf16_bits(x), to_bf16_bits(Bm), to_bf16_bits(Cm), to_bf16_bits(delta)
+    return SelectiveInputs(x=x, delta=delta, A=A, B=Bm, C=Cm, D=Dskip if with_D else None, init=h0,
+                           io_dtype=io_dtype, meta=dict(seed=seed, a_range=tuple(a_range)))
+
+
+def make_selective_config(name: str, seed: int = 0, **overrides) -> SelectiveInputs:
+    cfg = dict(SELECTIVE_CONFIGS[name])
+    cfg.update(overrides)
+    return make_selective_inputs(seed=seed, **cfg)
