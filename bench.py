@@ -34,11 +34,23 @@ METRIC = "SSD forward tokens/s on 1 GB300 + per-kernel % of HBM/tensor roofline"
 METRIC_DECODE = "SSD decode tokens/s on 1 GB300 + % of HBM roofline"
 
 
+METRIC_SEL = "Mamba-1 selective scan tokens/s on 1 GB300 + % of exp (MUFU) roofline"
+# one ex2 per (batch, token, channel, state) is the method's irreducible special-function work;
+# GB300: 152 SMs x 16 MUFU results per clock (4 per SM sub-partition) x 2.07 GHz, in G/s
+MUFU_PEAK_GPS = 152 * 16 * 2.07
+
+
 def is_decode(workload):
     return workload.startswith("decode")
 
 
+def is_selective(workload):
+    return workload.startswith("mamba1_")
+
+
 def metric_of(workload):
+    if is_selective(workload):
+        return METRIC_SEL
     return METRIC_DECODE if is_decode(workload) else METRIC
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
 
@@ -100,7 +112,7 @@ def load_peaks():
 def source_digest(kernel):
     files = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state_tc.cu",
              "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu",
-             "decode": "decode.cu"}
+             "decode": "decode.cu", "selective_scan": "selective_scan.cu"}
     p = os.path.join(ROOT, "state_space_model_02_gb300", "csrc", files[kernel])
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -191,6 +203,34 @@ def algorithmic_decode(shape):
     return by, fl
 
 
+def cpu_baseline_selective(inp, budget_s):
+    """The float64 selective-scan oracle on the host cores over a bounded sample: whole
+    sequences of as many channels as fit the time budget (tokens scaled to the layer)."""
+    from oracle import ref, selective
+
+    b, L, D = inp.x.shape
+    threads = ref.num_threads()
+
+    def run(nch):
+        sub = lambda a: np.ascontiguousarray(a[:, :, :nch])
+        t0 = time.perf_counter()
+        selective.selective_scan(sub(inp.x), sub(inp.delta), inp.A[:nch], inp.B, inp.C, inp.D[:nch],
+                                 None if inp.init is None else np.ascontiguousarray(inp.init[:, :nch]))
+        return time.perf_counter() - t0
+
+    probe = min(D, max(threads, 8))
+    per_ch = run(probe) / probe
+    nch = int(min(D, max(probe, budget_s / max(per_ch, 1e-9))))
+    reps, el = 0, 0.0
+    while reps == 0 or (el < budget_s and reps < 100):
+        el += run(nch)
+        reps += 1
+    tokens = reps * b * L * nch / D
+    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d channels x %d sequences of %d tokens x %d passes, float64, %.1f s"
+                      % (nch, D, b, L, reps, el)}
+
+
 def cpu_baseline(inp, budget_s):
     """The float64 oracle as it stands, on the host cores, over a bounded sample of the
     workload: whole (batch, head) sequences, as many as fit the time budget."""
@@ -239,13 +279,19 @@ def run_reference(args):
         return
     from state_space_model_02_gb300 import synth
 
-    inp = synth.make_config(args.workload, seed=args.seed)
-    shape = dict(synth.CONFIGS[args.workload])
+    if is_selective(args.workload):
+        inp = synth.make_selective_config(args.workload, seed=args.seed)
+        shape = dict(synth.SELECTIVE_CONFIGS[args.workload])
+        baseline = cpu_baseline_selective
+    else:
+        inp = synth.make_config(args.workload, seed=args.seed)
+        shape = dict(synth.CONFIGS[args.workload])
+        baseline = cpu_baseline
     vals = []
     per = max(1.0, args.cpu_seconds / max(1, args.steps))
     base = None
     for _ in range(args.steps):
-        base = cpu_baseline(inp, per)
+        base = baseline(inp, per)
         vals.append(base["value"])
     v = float(np.median(vals))
     tokens = shape["batch"] * shape["seqlen"]
@@ -275,6 +321,8 @@ def run_ours(args):
     cuda_build.build()
     ssd.load_library()
 
+    if is_selective(args.workload):
+        return run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev)
     shape = dict(synth.CONFIGS[args.workload])
     inp = synth.make_config(args.workload, seed=args.seed)
     bf16 = inp.io_dtype == "bf16"
@@ -443,6 +491,129 @@ def run_ours(args):
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in kern[n].items()}
                     for n in KERNELS},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": len(KERNELS) * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev):
+    """The Mamba-1 arm: one ssd_selective_scan launch per step over resident inputs."""
+    shape = dict(synth.SELECTIVE_CONFIGS[args.workload])
+    inp = synth.make_selective_config(args.workload, seed=args.seed)
+    bf16 = inp.io_dtype == "bf16"
+
+    def io(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else np.ascontiguousarray(a))
+        return t.view(torch.bfloat16) if bf16 else t
+
+    host = dict(x=io(inp.x), delta=io(inp.delta), B=io(inp.B), C=io(inp.C))
+    d = {k: v.to(dev) for k, v in host.items()}
+    A = torch.from_numpy(inp.A).to(dev)
+    Dk = torch.from_numpy(inp.D).to(dev)
+    init = None if inp.init is None else torch.from_numpy(inp.init).to(dev)
+    b, L, D, N = shape["batch"], shape["seqlen"], shape["dim"], shape["dstate"]
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((b, D, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(k):
+        flush.fill_(k & 0xFF)
+        flush_rd.max()
+
+    def step():
+        ssd.selective_scan(d["x"], d["delta"], A, d["B"], d["C"], Dk, init, y=y, final_state=fin,
+                           stream=stream)
+
+    for k in range(max(3, args.warmup)):
+        flush_l2(k)
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush_l2(k)
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = b * L
+    value = ws * tokens / (ms_step * 1e-3)
+    e = 2 if bf16 else 4
+    elems = b * L * D * N
+    hbm_bytes = 3 * b * L * D * e + 2 * b * L * N * e + D * N * 4 + D * 4 + (2 if init is not None else 1) * b * D * N * 4
+    ach = elems / (ms_step * 1e-3) / 1e9
+    roofline = {"kernel": "selective_scan", "bound": "alu", "achieved": ach, "peak": MUFU_PEAK_GPS,
+                "unit": "Gexp/s", "frac": ach / MUFU_PEAK_GPS, "traffic": profiled_traffic("selective_scan", args.workload),
+                "peak_source": "derived: 152 SMs x 16 MUFU ex2 per clock x 2.07 GHz (one exp per element)",
+                "hbm_context": {"bytes": hbm_bytes, "GBps": hbm_bytes / (ms_step * 1e-3) / 1e9}}
+
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            for k, v in pin.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            yy, _ = ssd.selective_scan(dev_in["x"], dev_in["delta"], A, dev_in["B"], dev_in["C"], Dk, init,
+                                       y=y, final_state=fin, stream=stream)
+            y_host.copy_(yy, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline_selective(inp, args.cpu_seconds)
+    line = {
+        "metric": METRIC_SEL, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": args.workload, **shape,
+                   "l2": "flushed before every step (256 MiB write + 256 MiB read, outside the timed events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": roofline,
+        "kernels": {"selective_scan": {"us": 1e3 * ms_step, "share": 1.0, "elements": elems,
+                                        "hbm_bytes": hbm_bytes}},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

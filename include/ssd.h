@@ -187,12 +187,44 @@ ssd_status ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const float* d
  *     state after the last token; it must not alias any input.
  *   - shape->chunk and shape->flags are ignored.  One launch reads and writes the state once,
  *     whatever seqlen is; the recurrence runs in float32.
- *   - Needs no workspace.  SSD_ERR_UNSUPPORTED unless dstate is a multiple of 64 with
- *     dstate / 64 <= 32, and headdim * dstate / 64 is a multiple of 32 and at most 512.
+ *   - Needs no workspace.  Supported shapes (else SSD_ERR_UNSUPPORTED): dstate in
+ *     {64, 128, 256, 512} with headdim a multiple of 8 and headdim * dstate a multiple of
+ *     1024; or dstate = 64 * 2^k <= 2048 with headdim * dstate / 64 a multiple of 32 and at
+ *     most 512.
  */
 ssd_status ssd_decode(const ssd_shape* shape, const void* x, const float* dt, const float* A,
                       const void* B, const void* C, const float* D, float* state, void* y,
                       void* stream);
+
+/*
+ * Mamba-1 selective scan, fused ("3.3 Hardware-aware algorithm and GPU memory hierarchy",
+ * booiljung.github.io, section 2.1: zero-order-hold discretisation Abar = exp(delta A),
+ * Bbar = (delta A)^-1 (exp(delta A) - I) delta B done on chip, only y written back; section 3:
+ * load, discretise, scan and read-out in one kernel; section 4.1: h_t = Abar_t h_{t-1} +
+ * Bbar_t x_t).  For every batch b, channel d < dim and state n < dstate, over t < seqlen:
+ *     h[d,n] <- exp(delta_t[d] A[d,n]) h[d,n] + (exp(delta_t[d] A[d,n]) - 1) / A[d,n] B_t[n] x_t[d]
+ *     y_t[d]  = sum_n C_t[n] h[d,n] + Dskip[d] x_t[d]
+ * (the factor is delta_t[d] B_t[n] x_t[d] where A[d,n] = 0).
+ *   - x, delta, y: (batch, seqlen, dim); B, C: (batch, seqlen, dstate); all in io_dtype.
+ *     A: float32 (dim, dstate); Dskip: float32 (dim), nullable (no skip term).
+ *   - init_state: float32 (batch, dim, dstate), nullable (zero state); final_state: float32
+ *     (batch, dim, dstate), nullable (not written); neither may alias another argument.
+ *   - Every pointer 16-byte aligned (SSD_ERR_ALIGN).  The recurrence runs in float32.
+ *   - Supported: dstate in {8, 16, 32, 64} and dim a multiple of 64 / dstate (else
+ *     SSD_ERR_UNSUPPORTED).  Needs no workspace; asynchronous on `stream`.
+ */
+typedef struct {
+  int64_t batch;    /* >= 1 */
+  int64_t seqlen;   /* >= 1 */
+  int64_t dim;      /* D: channels, >= 1 */
+  int64_t dstate;   /* N */
+  int32_t io_dtype; /* ssd_dtype of x, delta, B, C, y */
+  uint32_t flags;   /* reserved, 0 */
+} ssd_sel_shape;
+
+ssd_status ssd_selective_scan(const ssd_sel_shape* shape, const void* x, const void* delta,
+                              const float* A, const void* B, const void* C, const float* Dskip,
+                              const float* init_state, float* final_state, void* y, void* stream);
 
 /* Static description of a status code. */
 const char* ssd_status_str(ssd_status status);

@@ -359,6 +359,35 @@ ssd_status ssd_decode(const ssd_shape* shape, const void* x, const float* dt, co
   return SSD_OK;
 }
 
+ssd_status ssd_selective_scan(const ssd_sel_shape* shape, const void* x, const void* delta,
+                              const float* A, const void* B, const void* C, const float* Dskip,
+                              const float* init_state, float* final_state, void* y, void* stream) {
+  if (!shape) return fail(SSD_ERR_INVALID, "shape is null");
+  const ssd_sel_shape& s = *shape;
+  if (s.batch < 1 || s.seqlen < 1 || s.dim < 1 || s.dstate < 1)
+    return fail(SSD_ERR_INVALID, "every dimension must be >= 1");
+  if (s.io_dtype != SSD_F32 && s.io_dtype != SSD_BF16) return fail(SSD_ERR_INVALID, "bad io_dtype");
+  if (s.batch > 65535 || s.dim > (int64_t(1) << 20) || s.seqlen > (int64_t(1) << 31))
+    return fail(SSD_ERR_UNSUPPORTED, "dimension beyond the supported range");
+  ssd::SelProblem p{s.batch, s.seqlen, s.dim, s.dstate, s.io_dtype == SSD_BF16};
+  SSD_TRY(need(x, "x"));
+  SSD_TRY(need(delta, "delta"));
+  SSD_TRY(need(A, "A"));
+  SSD_TRY(need(B, "B"));
+  SSD_TRY(need(C, "C"));
+  SSD_TRY(need(y, "y"));
+  SSD_TRY(maybe(Dskip, "Dskip"));
+  SSD_TRY(maybe(init_state, "init_state"));
+  SSD_TRY(maybe(final_state, "final_state"));
+  if (!ssd::selective_ok(p))
+    return fail(SSD_ERR_UNSUPPORTED, "selective scan: dstate must be 8, 16, 32 or 64 and dim a multiple of 64/dstate");
+  const cudaError_t e = ssd::launch_selective_scan(p, x, delta, A, B, C, Dskip, init_state, final_state, y,
+                                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selective scan launch");
+  g_last_error[0] = '\0';
+  return SSD_OK;
+}
+
 const char* ssd_status_str(ssd_status s) {
   switch (s) {
     case SSD_OK: return "ok";

@@ -17,6 +17,12 @@ struct Problem {
   uint32_t flags;  // SSD_FLAG_*
 };
 
+// Mamba-1 selective scan: x, delta, y (b, L, D); B, C (b, L, N); A (D, N).
+struct SelProblem {
+  int64_t b, L, D, N;
+  bool io_bf16;
+};
+
 // Byte offsets inside the caller's workspace.  Each region is 1024-byte aligned.
 struct Layout {
   size_t status, cs2, dtT, S, hprev, total;
@@ -75,6 +81,12 @@ cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void*
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st);
+
+// Mamba-1 selective scan (fused zero-order hold + scan + read-out); applicability by selective_ok.
+bool selective_ok(const SelProblem& p);
+cudaError_t launch_selective_scan(const SelProblem& p, const void* x, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* Dskip, const float* init,
+                                  float* final_state, void* y, cudaStream_t st);
 
 // Recurrent form over a short run of tokens (decoding); applicability by decode_ok.
 bool decode_ok(const Problem& p);

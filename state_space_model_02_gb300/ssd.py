@@ -19,14 +19,19 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_E
 # Every entry point of include/ssd.h, in declaration order.
 EXPORTS = ("ssd_workspace_bytes", "ssd_get_workspace_layout", "ssd_fwd", "ssd_chunk_cumsum",
            "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_read_status",
-           "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_decode", "ssd_status_str",
-           "ssd_last_error", "ssd_kernel_plan")
+           "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_decode", "ssd_selective_scan",
+           "ssd_status_str", "ssd_last_error", "ssd_kernel_plan")
 
 
 class Shape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
                 ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk", ctypes.c_int64), ("io_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class SelShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -65,6 +70,7 @@ def load_library(path: str = LIB_PATH):
         "ssd_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ctypes.c_int),
         "ssd_fwd_noalloc": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "ssd_decode": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ssd_selective_scan": ([ctypes.POINTER(SelShape)] + [vp] * 10, ctypes.c_int),
         "ssd_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "ssd_last_error": ([], ctypes.c_char_p),
         "ssd_kernel_plan": ([sp], ctypes.c_int),
@@ -217,6 +223,40 @@ def decode(x, dt, A, B, C, D, state, *, y=None, stream=None):
     _check(load_library().ssd_decode(ctypes.byref(prob.c_shape()), _p(x), _p(dt), _p(A), _p(B), _p(C),
                                       _p(D), _p(state), _p(y), _stream(stream)))
     return y
+
+
+def selective_scan(x, delta, A, B, C, Dskip=None, init_state=None, *, y=None, final_state=None,
+                   want_final=True, stream=None):
+    """ssd_selective_scan (Mamba-1): returns (y, final_state or None).
+
+    x, delta (b,L,D) and B, C (b,L,N) in one dtype (bf16 or fp32); A (D,N), Dskip (D) and
+    init_state (b,D,N) in fp32.  Work is enqueued on ``stream`` (default: current).
+    """
+    torch = _torch()
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be (b, L, D) and B (b, L, N)")
+    b, L, D = x.shape
+    N = B.shape[2]
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype)
+    _need(delta, "delta", x.dtype, (b, L, D))
+    _need(B, "B", x.dtype, (b, L, N))
+    _need(C, "C", x.dtype, (b, L, N))
+    _need(A, "A", torch.float32, (D, N))
+    _need(Dskip, "Dskip", torch.float32, (D,))
+    _need(init_state, "init_state", torch.float32, (b, D, N))
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", x.dtype, x.shape)
+    if final_state is None and want_final:
+        final_state = torch.empty((b, D, N), dtype=torch.float32, device=x.device)
+    _need(final_state, "final_state", torch.float32, (b, D, N))
+    shape = SelShape(b, L, D, N, SSD_BF16 if x.dtype == torch.bfloat16 else SSD_F32, 0)
+    _check(load_library().ssd_selective_scan(ctypes.byref(shape), _p(x), _p(delta), _p(A), _p(B), _p(C),
+                                             _p(Dskip), _p(init_state), _p(final_state), _p(y),
+                                             _stream(stream)))
+    return y, final_state
 
 
 def chunk_cumsum(prob, dt, A, workspace, stream=None):

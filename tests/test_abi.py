@@ -139,3 +139,30 @@ def test_decode_rejects_bad_arguments_before_any_launch(lib):
     # the chunk field is not used by the recurrent form
     odd = shape(seqlen=1, chunk=100).c_shape()
     assert lib.ssd_decode(ctypes.byref(odd), *([None] * 8), None) == 1  # null x, not the chunk
+
+
+def test_selective_scan_rejects_bad_arguments_before_any_launch(lib):
+    good = ctypes.c_void_p(0x100000)
+    args = [good] * 5 + [None, None, None, good]   # x, delta, A, B, C, Dskip, init, final, y
+
+    def sh(**kw):
+        base = dict(batch=2, seqlen=64, dim=1536, dstate=16, io_dtype=ssd.SSD_BF16, flags=0)
+        base.update(kw)
+        return ssd.SelShape(**base)
+
+    assert lib.ssd_selective_scan(None, *args, None) == 1
+    assert lib.ssd_selective_scan(ctypes.byref(sh(seqlen=0)), *args, None) == 1
+    assert lib.ssd_selective_scan(ctypes.byref(sh(io_dtype=7)), *args, None) == 1
+    # state sizes outside {8, 16, 32, 64}; a channel count that does not fill whole warps
+    assert lib.ssd_selective_scan(ctypes.byref(sh(dstate=12)), *args, None) == 2
+    assert lib.ssd_selective_scan(ctypes.byref(sh(dstate=128)), *args, None) == 2
+    assert lib.ssd_selective_scan(ctypes.byref(sh(dim=1538)), *args, None) == 2
+    a = list(args)
+    a[0] = None
+    assert lib.ssd_selective_scan(ctypes.byref(sh()), *a, None) == 1
+    a = list(args)
+    a[3] = ctypes.c_void_p(0x100008)
+    assert lib.ssd_selective_scan(ctypes.byref(sh()), *a, None) == 3
+    a = list(args)
+    a[6] = ctypes.c_void_p(0x100004)   # misaligned init_state
+    assert lib.ssd_selective_scan(ctypes.byref(sh()), *a, None) == 3
