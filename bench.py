@@ -36,8 +36,9 @@ METRIC_DECODE = "SSD decode tokens/s on 1 GB300 + % of HBM roofline"
 
 METRIC_SEL = "Mamba-1 selective scan tokens/s on 1 GB300 + % of exp (MUFU) roofline"
 # one ex2 per (batch, token, channel, state) is the method's irreducible special-function work;
-# GB300: 152 SMs x 16 MUFU results per clock (4 per SM sub-partition) x 2.07 GHz, in G/s
-MUFU_PEAK_GPS = 152 * 16 * 2.07
+# GB300: 152 SMs x 32 MUFU results per clock (one warp instruction per SM per clock: the XU
+# pipe's peak as ncu accounts it) x 2.07 GHz, in G/s
+MUFU_PEAK_GPS = 152 * 32 * 2.07
 
 
 def is_decode(workload):
@@ -560,7 +561,7 @@ def run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev):
     ach = elems / (ms_step * 1e-3) / 1e9
     roofline = {"kernel": "selective_scan", "bound": "alu", "achieved": ach, "peak": MUFU_PEAK_GPS,
                 "unit": "Gexp/s", "frac": ach / MUFU_PEAK_GPS, "traffic": profiled_traffic("selective_scan", args.workload),
-                "peak_source": "derived: 152 SMs x 16 MUFU ex2 per clock x 2.07 GHz (one exp per element)",
+                "peak_source": "derived: 152 SMs x 32 MUFU ex2 per clock x 2.07 GHz (one exp per element)",
                 "hbm_context": {"bytes": hbm_bytes, "GBps": hbm_bytes / (ms_step * 1e-3) / 1e9}}
 
     e2e = None

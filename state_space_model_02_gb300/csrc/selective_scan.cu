@@ -22,12 +22,14 @@
 // warp -- delta and x of the warp's 64/N channels, B and C -- widened to float32 in shared
 // memory (the next block's loads are issued before the current block is processed).  Per
 // token each lane reads one float4 (its B and C pair) and one float2 (its channel's delta,
-// x), and runs the update on float32 pairs (fma.rn.f32x2): w = delta A, Abar = 2^(w log2 e)
-// (MUFU), and the zero-order-hold factor (exp(w) - 1) / A as delta (1 + w/2 + w^2/6 + w^3/24
-// + w^4/120) for |w| < 1/8 (where exp(w) - 1 would cancel) and (Abar - 1) / A above.
-// Each lane's two read-out products are summed, and the N / 2 lanes of a channel reduce
-// N / 2 tokens at a time with a recursive-halving exchange that leaves one token's y in
-// each lane.
+// x).  The state-independent work of N tokens -- z = delta A log2 e, Abar = 2^z (MUFU), the
+// zero-order-hold factor (exp(w) - 1) / A with w = z ln 2, taken as delta (1 + w/2 + w^2/6)
+// for |w| < 1/64 (where exp(w) - 1 would cancel) and as (Abar - 1) / A above, and
+// u = factor B x -- is done first, on float32 pairs (fma.rn.f32x2), so that N independent
+// chains hide the MUFU and shared-memory latencies; then the N dependent updates
+// h <- Abar h + u and the read-out shares C . h follow.  Each lane's two shares are summed,
+// and the N / 2 lanes of a channel reduce N / 2 tokens at a time with a recursive-halving
+// exchange that leaves one token's y in each lane.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(32) selective_scan_kernel(
   grid_dep_wait();  // inputs may come from the previous kernel in the stream
 
   const float2 Av = *reinterpret_cast<const float2*>(A + d * N + 2 * p);
-  const float2 invA = make_float2(1.f / Av.x, 1.f / Av.y);  // unused where A = 0 (|w| < 1/8)
+  const float2 invA = make_float2(1.f / Av.x, 1.f / Av.y);  // unused where A = 0 (|w| < 1/64)
   float2 h = make_float2(0.f, 0.f);
   if (init) h = *reinterpret_cast<const float2*>(init + (b * D + d) * N + 2 * p);
   const float dsk = (Dskip && p == 0) ? __ldg(Dskip + d) : 0.f;
@@ -164,33 +166,46 @@ __global__ void __launch_bounds__(32) selective_scan_kernel(
   }
   __syncwarp();
 
-  const float2 l2e = make_float2(kLog2eSel, kLog2eSel);
-  const float2 p1 = make_float2(1.f, 1.f), p2 = make_float2(0.5f, 0.5f);
-  const float2 p3 = make_float2(1.f / 6.f, 1.f / 6.f), p4 = make_float2(1.f / 24.f, 1.f / 24.f);
-  const float2 p5 = make_float2(1.f / 120.f, 1.f / 120.f);
   const float2 ninvA = make_float2(-invA.x, -invA.y);
+  const float2 a2z = make_float2(Av.x * kLog2eSel, Av.y * kLog2eSel);  // exp(delta A) = 2^(delta a2z)
+  // the hold's factor for small |w| as a polynomial in z = w log2 e: 1 + (ln2/2) z + (ln2^2/6) z^2
+  const float2 one = make_float2(1.f, 1.f);
+  const float2 k1z = make_float2(0.34657359027997264f, 0.34657359027997264f);
+  const float2 k2z = make_float2(0.08007410688212759f, 0.08007410688212759f);
+  constexpr float kZSmall = 0.022541950359959f;  // |w| < 1/64
 
-  // one token: update the lane's two states, return its share of y_t[d]
-  auto step = [&](const float* rowp) -> float {
+  // the state-independent work of a token: Abar and u = Bbar x for the lane's two states, its
+  // C pair and the skip term
+  struct Pre {
+    float2 ab, u, cc;
+    float sx;
+  };
+  auto prepare = [&](const float* rowp) -> Pre {
     const float4 bc = *reinterpret_cast<const float4*>(rowp + Geo::kBC + 4 * p);
     const float2 dx = *reinterpret_cast<const float2*>(rowp + Geo::kDX + 2 * c);
     const float2 dl2 = make_float2(dx.x, dx.x);
-    const float2 w = mul_f32x2(dl2, Av);
-    const float2 z = mul_f32x2(w, l2e);
+    const float2 z = mul_f32x2(dl2, a2z);
     const float2 ab = make_float2(ex2(z.x), ex2(z.y));
-    // zero-order-hold factor (exp(w) - 1) / A
-    float2 e = fma_f32x2(w, p5, p4);
-    e = fma_f32x2(w, e, p3);
-    e = fma_f32x2(w, e, p2);
-    e = fma_f32x2(w, e, p1);
+    const float2 e = fma_f32x2(z, fma_f32x2(z, k2z, k1z), one);
     const float2 cs = mul_f32x2(dl2, e);
     const float2 cl = fma_f32x2(ab, invA, ninvA);
-    const float2 cf = make_float2(fabsf(w.x) < 0.125f ? cs.x : cl.x, fabsf(w.y) < 0.125f ? cs.y : cl.y);
+    const float2 cf = make_float2(fabsf(z.x) < kZSmall ? cs.x : cl.x, fabsf(z.y) < kZSmall ? cs.y : cl.y);
     const float2 u = mul_f32x2(cf, mul_f32x2(make_float2(bc.x, bc.y), make_float2(dx.y, dx.y)));
-    h = fma_f32x2(ab, h, u);
-    const float2 yc = mul_f32x2(make_float2(bc.z, bc.w), h);
-    return fmaf(dsk, dx.y, yc.x + yc.y);  // Dskip x enters once per channel (lane p = 0)
+    Pre r;
+    r.ab = ab;
+    r.u = u;
+    r.cc = make_float2(bc.z, bc.w);
+    r.sx = dsk * dx.y;  // Dskip x enters once per channel (lane p = 0)
+    return r;
   };
+
+  // the sequential part: h <- Abar h + u, and the lane's share of y_t
+  auto advance = [&](const Pre& r) -> float {
+    h = fma_f32x2(r.ab, h, r.u);
+    const float2 yc = mul_f32x2(r.cc, h);
+    return r.sx + (yc.x + yc.y);
+  };
+  auto step = [&](const float* rowp) -> float { return advance(prepare(rowp)); };
 
   for (int64_t t0 = 0, blk = 0; t0 < L; t0 += TB, ++blk) {
     const int nt = static_cast<int>(L - t0 < TB ? L - t0 : TB);
@@ -205,11 +220,15 @@ __global__ void __launch_bounds__(32) selective_scan_kernel(
     // flight at once
     int tb = 0;
     for (; tb + 2 * W <= nt; tb += 2 * W) {
+      // the state-independent work of all 2W tokens first, then the dependent updates
       float pa[W], pb[W];
+      Pre pr[2 * W];
 #pragma unroll
-      for (int k = 0; k < W; ++k) pa[k] = step(rows + (tb + k) * RF);
+      for (int k = 0; k < 2 * W; ++k) pr[k] = prepare(rows + (tb + k) * RF);
 #pragma unroll
-      for (int k = 0; k < W; ++k) pb[k] = step(rows + (tb + W + k) * RF);
+      for (int k = 0; k < W; ++k) pa[k] = advance(pr[k]);
+#pragma unroll
+      for (int k = 0; k < W; ++k) pb[k] = advance(pr[W + k]);
       const int ia = reduce_scatter_group<W>(pa, lane);
       const int ib = reduce_scatter_group<W>(pb, lane);
       st_out(y + (b * L + t0 + tb + ia) * D + d, pa[0]);
