@@ -20,6 +20,10 @@ namespace ssd {
 namespace {
 
 constexpr int kDepth = 8;
+// bf16x8 kernel: 64-thread CTAs and at most 56 registers (18 CTAs per SM), so that a layer's
+// columns fit in one wave of evenly loaded SMs (each thread walks all chunks of its column:
+// a second, partial wave would take as long as the first)
+constexpr int kDepth8 = 5, kBf16x8Threads = 64, kBf16x8MinCtas = 18;
 
 __device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
 __device__ __forceinline__ float4 load4(const float* src) { return __ldcs(reinterpret_cast<const float4*>(src)); }
@@ -39,7 +43,7 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
 }
 
 // bf16 S / hprev, 8 elements per thread.
-__global__ void __launch_bounds__(256, 4) state_passing_bf16x8_kernel(
+__global__ void __launch_bounds__(kBf16x8Threads, kBf16x8MinCtas) state_passing_bf16x8_kernel(
     const uint16_t* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     uint16_t* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN,
     int64_t nc, int64_t Q, int64_t total8) {
@@ -66,12 +70,12 @@ __global__ void __launch_bounds__(256, 4) state_passing_bf16x8_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) hv[i] = 0.f;
   }
-  uint4 sbuf[kDepth];
-  float dbuf[kDepth];
+  uint4 sbuf[kDepth8];
+  float dbuf[kDepth8];
   const uint16_t* sp = S + (bi * nc * H + h) * PN + e;
   const float* dp = cs2 + bh * nc * Q + (Q - 1);
 #pragma unroll
-  for (int k = 0; k < kDepth; ++k) {
+  for (int k = 0; k < kDepth8; ++k) {
     if (k < n) {
       sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
       dbuf[k] = __ldg(dp);
@@ -79,9 +83,9 @@ __global__ void __launch_bounds__(256, 4) state_passing_bf16x8_kernel(
       dp += Q;
     }
   }
-  for (int c0 = 0; c0 < n; c0 += kDepth) {
+  for (int c0 = 0; c0 < n; c0 += kDepth8) {
 #pragma unroll
-    for (int k = 0; k < kDepth; ++k) {
+    for (int k = 0; k < kDepth8; ++k) {
       const int c = c0 + k;
       if (c < n) {
         uint4 o;
@@ -92,13 +96,15 @@ __global__ void __launch_bounds__(256, 4) state_passing_bf16x8_kernel(
         *reinterpret_cast<uint4*>(Hp) = o;
         Hp += cstride;
         const float d = ex2(dbuf[k]);
-        const uint32_t w[4] = {sbuf[k].x, sbuf[k].y, sbuf[k].z, sbuf[k].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          hv[2 * i] = fmaf(d, hv[2 * i], bf16lo_to_f32(w[i]));
-          hv[2 * i + 1] = fmaf(d, hv[2 * i + 1], bf16hi_to_f32(w[i]));
-        }
-        if (c + kDepth < n) {  // refill this ring entry with chunk c + kDepth
+        hv[0] = fmaf(d, hv[0], bf16lo_to_f32(sbuf[k].x));
+        hv[1] = fmaf(d, hv[1], bf16hi_to_f32(sbuf[k].x));
+        hv[2] = fmaf(d, hv[2], bf16lo_to_f32(sbuf[k].y));
+        hv[3] = fmaf(d, hv[3], bf16hi_to_f32(sbuf[k].y));
+        hv[4] = fmaf(d, hv[4], bf16lo_to_f32(sbuf[k].z));
+        hv[5] = fmaf(d, hv[5], bf16hi_to_f32(sbuf[k].z));
+        hv[6] = fmaf(d, hv[6], bf16lo_to_f32(sbuf[k].w));
+        hv[7] = fmaf(d, hv[7], bf16hi_to_f32(sbuf[k].w));
+        if (c + kDepth8 < n) {  // refill this ring entry with chunk c + kDepth8
           sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
           dbuf[k] = __ldg(dp);
           sp += cstride;
@@ -213,8 +219,8 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
   const int64_t PN = p.P * p.N;
   if (p.io_bf16 && PN % 8 == 0) {
     const int64_t total8 = p.b * p.H * (PN / 8);
-    const unsigned blocks8 = static_cast<unsigned>((total8 + 255) / 256);
-    return launch_pdl(state_passing_bf16x8_kernel, dim3(blocks8), dim3(256), 0, st,
+    const unsigned blocks8 = static_cast<unsigned>((total8 + kBf16x8Threads - 1) / kBf16x8Threads);
+    return launch_pdl(state_passing_bf16x8_kernel, dim3(blocks8), dim3(kBf16x8Threads), 0, st,
                       static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev),
                       final_state, p.H, PN, p.nc, p.Q, total8);
   }
