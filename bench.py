@@ -267,6 +267,22 @@ def cpu_baseline(inp, budget_s):
 # ------------------------------------------------------------------------------ arms
 
 
+def max_over_ranks(ms, ws, dist, dev):
+    """The job's time for a quantity every rank measured: the slowest rank's (MAX all-reduce)."""
+    if ws <= 1:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_per_rank, ws, ms):
+    """Whole-job throughput: every rank's tokens over the job's (slowest rank's) time."""
+    return ws * tokens_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -406,12 +422,9 @@ def run_ours(args):
     for e in evs:
         for i, n in enumerate(KERNELS):
             per_kernel[n].append(e[i].elapsed_time(e[i + 1]))
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, ws, dist, dev)
     tokens = prob.batch * prob.seqlen
-    value = ws * tokens / (ms_step * 1e-3)
+    value = job_rate(tokens, ws, ms_step)
 
     # roofline of every kernel; the dominant (largest share) is reported
     by, fl = algorithmic(shape)
@@ -464,11 +477,8 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+        ms_e2e = max_over_ranks(ms_e2e, ws, dist, dev)
+        e2e = {"value": job_rate(tokens, ws, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:
@@ -549,12 +559,9 @@ def run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev):
     if ws > 1:
         dist.barrier()
     ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, ws, dist, dev)
     tokens = b * L
-    value = ws * tokens / (ms_step * 1e-3)
+    value = job_rate(tokens, ws, ms_step)
     e = 2 if bf16 else 4
     elems = b * L * D * N
     hbm_bytes = 3 * b * L * D * e + 2 * b * L * N * e + D * N * 4 + D * 4 + (2 if init is not None else 1) * b * D * N * 4
@@ -589,11 +596,8 @@ def run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev):
         e1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+        ms_e2e = max_over_ranks(ms_e2e, ws, dist, dev)
+        e2e = {"value": job_rate(tokens, ws, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:
@@ -659,12 +663,9 @@ def run_decode(args, torch, dist, ssd, ws, rank, local, dev, shape, inp, host, d
     if ws > 1:
         dist.barrier()
     ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, ws, dist, dev)
     tokens = b * T
-    value = ws * tokens / (ms_step * 1e-3)
+    value = job_rate(tokens, ws, ms_step)
     by, fl = algorithmic_decode(shape)
     peaks = load_peaks()
     ach = by / (ms_step * 1e-3) / 1e9
@@ -700,11 +701,8 @@ def run_decode(args, torch, dist, ssd, ws, rank, local, dev, shape, inp, host, d
         e1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": ws * tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+        ms_e2e = max_over_ranks(ms_e2e, ws, dist, dev)
+        e2e = {"value": job_rate(tokens, ws, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "note": "state resident on the device across steps"}
 
