@@ -226,6 +226,34 @@ ssd_status ssd_selective_scan(const ssd_sel_shape* shape, const void* x, const v
                               const float* A, const void* B, const void* C, const float* Dskip,
                               const float* init_state, float* final_state, void* y, void* stream);
 
+/*
+ * Backward pass of ssd_fwd: the gradients of a loss w.r.t. every input of the forward scan,
+ * given dL/dy and dL/dfinal_state.  For the recurrence h_t = a_t h_{t-1} + dt_t x_t (x) B_t,
+ * a_t = exp(dt_t A), y_t = h_t C_t + D x_t ("Mamba-2 cuda-tile forward pass kernels" sections
+ * 1-2), the adjoint state g_t = dL/dh_t obeys g_t = dy_t (x) C_t + a_{t+1} g_{t+1}: the same
+ * kind of scan in reversed time.  The library runs five scans through the forward kernels (the
+ * forward again without D; the adjoint scan, read out with B; a role-swapped forward scan for
+ * dC and a role-swapped reversed scan for dB, both with head dim dstate and state headdim)
+ * and element-wise / reduction kernels between them:
+ *     dx = dt (g B) + D dy,  dB = sum_heads dt g^T x,  dC = sum_heads h^T dy,  dD = sum <dy, x>,
+ *     dinit = a_0 g_0,  ddt = <x, g B> + A r,  dA = sum dt r,
+ * with r_t = sum_{s >= t} (<dy_s, y_s - D x_s> - dt_s <x_s, g_s B_s>) (+ <dfinal, final> at the
+ * last token), the derivative along the running sum of A dt that every decay depends on.
+ *   - Inputs as for ssd_fwd; dy in the I/O dtype with y's shape; dfinal float32
+ *     (batch, nheads, headdim, dstate), nullable (zero).
+ *   - Outputs: dx (x's shape, I/O dtype), ddt float32 (batch, seqlen, nheads), dA float32
+ *     (nheads), dB and dC (B's shape, I/O dtype), dD float32 (nheads, nullable: not written),
+ *     dinit float32 (init's shape, nullable: not written).  No output may alias an input.
+ *   - workspace: at least ssd_bwd_workspace_bytes(shape), 256-byte aligned, caller-owned.
+ *   - Precision follows the I/O dtype: with bf16 I/O the scans' inputs and outputs are bf16
+ *     and their arithmetic float32, as in the forward.
+ */
+size_t ssd_bwd_workspace_bytes(const ssd_shape* shape);
+ssd_status ssd_bwd(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* B,
+                   const void* C, const float* D, const float* init_state, const void* dy,
+                   const float* dfinal, void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
+                   float* dinit, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static description of a status code. */
 const char* ssd_status_str(ssd_status status);
 

@@ -20,12 +20,14 @@ namespace {
 constexpr int kHeadsPerCta = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// unit_scale: dtT holds 1 for every token of the sequence (0 past its end) instead of dt --
+// the scan whose inputs are not scaled by the step, which the backward pass runs.
 template <int Q>
 __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restrict__ dt,
                                                            const float* __restrict__ A,
                                                            float* __restrict__ cs2,
                                                            float* __restrict__ dtT, int64_t L,
-                                                           int64_t H, int64_t nc) {
+                                                           int64_t H, int64_t nc, bool unit_scale) {
   constexpr int R = Q / 32;                 // tokens per lane
   constexpr int ROW = Q + Q / 32;           // padded row (t + t/32) for the staging writes
   __shared__ float tile[kHeadsPerCta][ROW];
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
       if (lane >= off) incl += o;
     }
     out_cs[t] = (carry + incl) * kLog2e;
-    out_dt[t] = d;
+    out_dt[t] = unit_scale ? (c * Q + t < L ? 1.f : 0.f) : d;
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
@@ -78,16 +80,16 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
-                                float* dtT, cudaStream_t st) {
+                                float* dtT, cudaStream_t st, bool unit_scale) {
   const dim3 grid(static_cast<unsigned>(p.nc), static_cast<unsigned>(p.b),
                   static_cast<unsigned>((p.H + kHeadsPerCta - 1) / kHeadsPerCta));
   switch (p.Q) {
     case 64:
-      return launch_pdl(chunk_cumsum_kernel<64>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
+      return launch_pdl(chunk_cumsum_kernel<64>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc, unit_scale);
     case 128:
-      return launch_pdl(chunk_cumsum_kernel<128>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
+      return launch_pdl(chunk_cumsum_kernel<128>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc, unit_scale);
     case 256:
-      return launch_pdl(chunk_cumsum_kernel<256>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc);
+      return launch_pdl(chunk_cumsum_kernel<256>, grid, dim3(256), 0, st, dt, A, cs2, dtT, p.L, p.H, p.nc, unit_scale);
     default:
       return cudaErrorInvalidValue;
   }

@@ -90,8 +90,8 @@ bool use_scan_tc(const ssd::Problem& p) {
 // ---- the four steps on an already checked problem ----
 
 ssd_status step_cumsum(const ssd::Problem& p, const float* dt, const float* A, const Views& v,
-                       cudaStream_t st) {
-  const cudaError_t e = ssd::launch_chunk_cumsum(p, dt, A, v.cs2, v.dtT, st);
+                       cudaStream_t st, bool unit_scale = false) {
+  const cudaError_t e = ssd::launch_chunk_cumsum(p, dt, A, v.cs2, v.dtT, st, unit_scale);
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_cumsum launch");
 }
 
@@ -384,6 +384,168 @@ ssd_status ssd_selective_scan(const ssd_sel_shape* shape, const void* x, const v
   const cudaError_t e = ssd::launch_selective_scan(p, x, delta, A, B, C, Dskip, init_state, final_state, y,
                                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "selective scan launch");
+  g_last_error[0] = '\0';
+  return SSD_OK;
+}
+
+// ---------------------------------------------------------------------------- backward
+
+namespace {
+
+// Regions of the backward workspace (each 256-byte aligned).
+struct BwdLayout {
+  size_t scan, y, fin, xin, bin, cin, dtr, init, out, fin1, dcs, xgb, dap, total;
+};
+
+// The transposed problem of the two role-swapped scans: head dim N, state P, one group per head.
+ssd_shape swapped_shape(const ssd_shape& s) {
+  ssd_shape t = s;
+  t.headdim = s.dstate;
+  t.dstate = s.headdim;
+  t.ngroups = s.nheads;
+  t.flags = 0;
+  return t;
+}
+
+bool bwd_layout(const ssd_shape* shape, BwdLayout* l) {
+  ssd::Problem p, q;
+  if (make_problem(shape, &p) != SSD_OK) return false;
+  const ssd_shape sw = swapped_shape(*shape);
+  if (make_problem(&sw, &q) != SSD_OK) return false;
+  ssd::Problem pf = p;  // the float32 scans
+  pf.io_bf16 = false;
+  const size_t e = 4;   // every scan buffer is sized for float32
+  const size_t BL = size_t(p.b * p.L), PN = size_t(p.P * p.N);
+  const size_t F = size_t(p.P > p.N ? p.P : p.N);
+  const size_t wide = size_t(p.G * p.N > p.H * p.P ? p.G * p.N : p.H * p.P);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = ssd::align_up(o + bytes, 256); return at; };
+  const size_t w1 = ssd::make_layout(pf).total, w2 = ssd::make_layout(q).total;
+  l->scan = take(w1 > w2 ? w1 : w2);
+  l->y = take(BL * p.H * p.P * e);
+  l->fin = take(size_t(p.b * p.H) * PN * 4);
+  l->xin = take(BL * p.H * F * e);
+  l->bin = take(BL * wide * e);
+  l->cin = take(BL * wide * e);
+  l->dtr = take(BL * p.H * 4);
+  l->init = take(size_t(p.b * p.H) * PN * 4);
+  l->out = take(BL * p.H * F * e);
+  l->fin1 = take(size_t(p.b * p.H) * PN * 4);
+  l->dcs = take(BL * p.H * 4);
+  l->xgb = take(BL * p.H * 4);
+  l->dap = take(size_t(p.b * p.H) * 4);
+  l->total = o;
+  return true;
+}
+
+// One forward scan (the four steps) of problem p over caller buffers, on workspace ws.
+ssd_status run_scan(const ssd::Problem& p, void* ws, const void* x, const float* dt, const float* A,
+                    const void* B, const void* C, const float* init, void* y, float* final_state,
+                    bool unit_scale, cudaStream_t st) {
+  Views v;
+  SSD_TRY(carve(p, ws, ssd::make_layout(p).total, &v));
+  SSD_TRY(step_cumsum(p, dt, A, v, st, unit_scale));
+  SSD_TRY(step_state(p, x, B, v, st));
+  SSD_TRY(step_passing(p, init, final_state, v, st));
+  return step_scan(p, x, B, C, nullptr, y, v, st);
+}
+
+ssd_status cuda_ok(cudaError_t e, const char* where) { return e == cudaSuccess ? SSD_OK : cuda_fail(e, where); }
+
+}  // namespace
+
+size_t ssd_bwd_workspace_bytes(const ssd_shape* shape) {
+  BwdLayout l;
+  return bwd_layout(shape, &l) ? l.total : 0;
+}
+
+ssd_status ssd_bwd(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* B,
+                   const void* C, const float* D, const float* init_state, const void* dy,
+                   const float* dfinal, void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
+                   float* dinit, void* workspace, size_t workspace_bytes, void* stream) {
+  ssd::Problem p;
+  SSD_TRY(make_problem(shape, &p));
+  SSD_TRY(need(x, "x"));
+  SSD_TRY(need(dt, "dt"));
+  SSD_TRY(need(A, "A"));
+  SSD_TRY(need(B, "B"));
+  SSD_TRY(need(C, "C"));
+  SSD_TRY(need(dy, "dy"));
+  SSD_TRY(need(dx, "dx"));
+  SSD_TRY(need(ddt, "ddt"));
+  SSD_TRY(need(dA, "dA"));
+  SSD_TRY(need(dB, "dB"));
+  SSD_TRY(need(dC, "dC"));
+  SSD_TRY(maybe(D, "D"));
+  SSD_TRY(maybe(init_state, "init_state"));
+  SSD_TRY(maybe(dfinal, "dfinal"));
+  SSD_TRY(maybe(dD, "dD"));
+  SSD_TRY(maybe(dinit, "dinit"));
+  BwdLayout l;
+  if (!bwd_layout(shape, &l)) return fail(SSD_ERR_INVALID, "backward: bad shape");
+  if (!workspace) return fail(SSD_ERR_WORKSPACE, "workspace is null");
+  if (workspace_bytes < l.total) return fail(SSD_ERR_WORKSPACE, "workspace smaller than ssd_bwd_workspace_bytes()");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(SSD_ERR_ALIGN, "workspace must be 256-byte aligned");
+  ssd::Problem q;
+  const ssd_shape sw = swapped_shape(*shape);
+  SSD_TRY(make_problem(&sw, &q));
+  char* w = static_cast<char*>(workspace);
+  void* ws_scan = w + l.scan;
+  void* t_y = w + l.y;
+  float* t_fin = reinterpret_cast<float*>(w + l.fin);
+  void* t_x = w + l.xin;
+  void* t_b = w + l.bin;
+  void* t_c = w + l.cin;
+  float* t_dtr = reinterpret_cast<float*>(w + l.dtr);
+  float* t_init = reinterpret_cast<float*>(w + l.init);
+  void* t_out = w + l.out;
+  float* t_fin1 = reinterpret_cast<float*>(w + l.fin1);
+  float* t_dcs = reinterpret_cast<float*>(w + l.dcs);
+  float* t_xgb = reinterpret_cast<float*>(w + l.xgb);
+  float* t_dap = reinterpret_cast<float*>(w + l.dap);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t e = p.io_bf16 ? 2 : 4;
+  const bool bf = p.io_bf16;
+  ssd::Problem pf = p;
+  pf.io_bf16 = false;
+  float* fx = static_cast<float*>(t_x);
+  float* fb = static_cast<float*>(t_b);
+  float* fc = static_cast<float*>(t_c);
+  float* fy = static_cast<float*>(t_y);
+  float* fo = static_cast<float*>(t_out);
+  SSD_TRY(cuda_ok(cudaMemsetAsync(ws_scan, 0, sizeof(uint32_t), st), "status reset"));
+
+  // 1. the forward again in float32, without the skip term: y - D x and the final state
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(x, fx, p.b, p.L, p.H, p.H, p.P, false, bf, st), "widen"));
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(B, fb, p.b, p.L, p.G, p.G, p.N, false, bf, st), "widen"));
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(C, fc, p.b, p.L, p.G, p.G, p.N, false, bf, st), "widen"));
+  SSD_TRY(run_scan(pf, ws_scan, fx, dt, A, fb, fc, init_state, fy, t_fin, false, st));
+  // 2. the adjoint scan in reversed time, in float32: x <- dy, B <- C, C <- B, decays shifted
+  //    by one token, inputs unscaled, starting from dfinal; its output is g B, its final
+  //    state g_0
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(dy, fx, p.b, p.L, p.H, p.H, p.P, true, bf, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(C, fb, p.b, p.L, p.G, p.G, p.N, true, bf, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_widen_flip_expand(B, fc, p.b, p.L, p.G, p.G, p.N, true, bf, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_reverse_decay(dt, t_dtr, p.b, p.L, p.H, st), "reverse decay"));
+  SSD_TRY(run_scan(pf, ws_scan, fx, t_dtr, A, fb, fc, dfinal, fo, t_fin1, true, st));
+  // 3. dx, dL/dcs, ddt, dA, dD, dinit
+  SSD_TRY(cuda_ok(ssd::launch_bwd_combine(p, dy, x, fy, fo, dt, D, dx, t_dcs, t_xgb, st), "combine"));
+  SSD_TRY(cuda_ok(ssd::launch_bwd_scalars(p, dfinal, t_fin, t_xgb, dt, A, t_dcs, ddt, t_dap, dA, st), "scalars"));
+  if (dinit) SSD_TRY(cuda_ok(ssd::launch_dinit(p, t_fin1, dt, A, dinit, st), "dinit"));
+  if (dD) SSD_TRY(cuda_ok(ssd::launch_dD(p, dy, x, dD, st), "dD"));
+  // 4. dC: forward scan with x <- B (per head), B <- x, C <- dy, from init^T; summed per group
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(B, t_x, p.b, p.L, p.G, p.H, p.N * e, false, st), "expand"));
+  if (init_state) SSD_TRY(cuda_ok(ssd::launch_transpose_state(init_state, t_init, p.b * p.H, p.P, p.N, st), "transpose"));
+  SSD_TRY(run_scan(q, ws_scan, t_x, dt, A, x, dy, init_state ? t_init : nullptr, t_out, nullptr, false, st));
+  SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, nullptr, dC, p.N, false, st), "group sum"));
+  // 5. dB: reversed scan with x <- C (per head), B <- dy, C <- x, from dfinal^T; times dt,
+  //    summed per group
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(C, t_x, p.b, p.L, p.G, p.H, p.N * e, true, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(dy, t_b, p.b, p.L, p.H, p.H, p.P * e, true, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(x, t_c, p.b, p.L, p.H, p.H, p.P * e, true, st), "flip"));
+  if (dfinal) SSD_TRY(cuda_ok(ssd::launch_transpose_state(dfinal, t_init, p.b * p.H, p.P, p.N, st), "transpose"));
+  SSD_TRY(run_scan(q, ws_scan, t_x, t_dtr, A, t_b, t_c, dfinal ? t_init : nullptr, t_out, nullptr, true, st));
+  SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, dt, dB, p.N, true, st), "group sum"));
   g_last_error[0] = '\0';
   return SSD_OK;
 }

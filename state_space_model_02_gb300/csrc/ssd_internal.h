@@ -69,7 +69,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // ---- launchers (each returns the launch's cudaError_t; none synchronises) ----
 
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
-                                float* dtT, cudaStream_t st);
+                                float* dtT, cudaStream_t st, bool unit_scale = false);
 
 cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,
@@ -81,6 +81,24 @@ cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void*
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st);
+
+// Backward pass: the steps between its scans (backward.cu).
+cudaError_t launch_flip_expand(const void* src, void* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
+                               int64_t row_bytes, bool flip, cudaStream_t st);
+cudaError_t launch_reverse_decay(const float* dt, float* out, int64_t b, int64_t L, int64_t H, cudaStream_t st);
+cudaError_t launch_transpose_state(const float* src, float* dst, int64_t rows, int64_t P, int64_t N, cudaStream_t st);
+cudaError_t launch_widen_flip_expand(const void* src, float* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
+                                     int64_t F, bool flip, bool src_bf16, cudaStream_t st);
+cudaError_t launch_bwd_combine(const Problem& p, const void* dy, const void* x, const float* yssm, const float* gB_rev,
+                               const float* dt, const float* D, void* dx, float* dcs, float* xgB, cudaStream_t st);
+cudaError_t launch_bwd_scalars(const Problem& p, const float* dfinal, const float* fin, const float* xgB,
+                               const float* dt, const float* A, float* dcs, float* ddt, float* dA_part, float* dA,
+                               cudaStream_t st);
+cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t N, bool flip,
+                             cudaStream_t st);
+cudaError_t launch_dinit(const Problem& p, const float* g0, const float* dt, const float* A, float* dinit,
+                         cudaStream_t st);
+cudaError_t launch_dD(const Problem& p, const void* dy, const void* x, float* dD, cudaStream_t st);
 
 // Mamba-1 selective scan (fused zero-order hold + scan + read-out); applicability by selective_ok.
 bool selective_ok(const SelProblem& p);

@@ -20,6 +20,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_E
 EXPORTS = ("ssd_workspace_bytes", "ssd_get_workspace_layout", "ssd_fwd", "ssd_chunk_cumsum",
            "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_read_status",
            "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_decode", "ssd_selective_scan",
+           "ssd_bwd_workspace_bytes", "ssd_bwd",
            "ssd_status_str", "ssd_last_error", "ssd_kernel_plan")
 
 
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH):
         "ssd_fwd_noalloc": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "ssd_decode": ([sp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "ssd_selective_scan": ([ctypes.POINTER(SelShape)] + [vp] * 10, ctypes.c_int),
+        "ssd_bwd_workspace_bytes": ([sp], ctypes.c_size_t),
+        "ssd_bwd": ([sp] + [vp] * 17 + [ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_status_str": ([ctypes.c_int], ctypes.c_char_p),
         "ssd_last_error": ([], ctypes.c_char_p),
         "ssd_kernel_plan": ([sp], ctypes.c_int),
@@ -257,6 +260,38 @@ def selective_scan(x, delta, A, B, C, Dskip=None, init_state=None, *, y=None, fi
                                              _p(Dskip), _p(init_state), _p(final_state), _p(y),
                                              _stream(stream)))
     return y, final_state
+
+
+def bwd(x, dt, A, B, C, D, dy, chunk=256, init_state=None, dfinal=None, *, workspace=None, stream=None,
+        flags=0):
+    """ssd_bwd: gradients of the forward scan given dy (and dfinal).  Returns a dict with
+    dx, ddt, dA, dB, dC, dD and dinit (None when init_state is None)."""
+    torch = _torch()
+    prob = problem_of(x, B, chunk, flags)
+    b, L, H, P, N, G = prob.batch, prob.seqlen, prob.nheads, prob.headdim, prob.dstate, prob.ngroups
+    _need(x, "x", x.dtype)
+    _need(B, "B", x.dtype, (b, L, G, N))
+    _need(C, "C", x.dtype, (b, L, G, N))
+    _need(dy, "dy", x.dtype, x.shape)
+    _need(dt, "dt", torch.float32, (b, L, H))
+    _need(A, "A", torch.float32, (H,))
+    _need(D, "D", torch.float32, (H,))
+    _need(init_state, "init_state", torch.float32, (b, H, P, N))
+    _need(dfinal, "dfinal", torch.float32, (b, H, P, N))
+    lib = load_library()
+    nbytes = lib.ssd_bwd_workspace_bytes(ctypes.byref(prob.c_shape()))
+    if nbytes == 0:
+        raise SSDError(1, "bad shape")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    out = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A), dB=torch.empty_like(B),
+               dC=torch.empty_like(C), dD=torch.empty(H, dtype=torch.float32, device=x.device),
+               dinit=None if init_state is None else torch.empty_like(init_state))
+    _check(lib.ssd_bwd(ctypes.byref(prob.c_shape()), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(init_state),
+                       _p(dy), _p(dfinal), _p(out["dx"]), _p(out["ddt"]), _p(out["dA"]), _p(out["dB"]),
+                       _p(out["dC"]), _p(out["dD"]), _p(out["dinit"]), _p(workspace), workspace.numel(),
+                       _stream(stream)))
+    return out
 
 
 def chunk_cumsum(prob, dt, A, workspace, stream=None):
