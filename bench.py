@@ -49,10 +49,28 @@ def is_selective(workload):
     return workload.startswith("mamba1_")
 
 
+METRIC_BWD = "SSD backward tokens/s on 1 GB300 + % of HBM roofline"
+
+
+def is_bwd(workload):
+    return workload.startswith("bwd_")
+
+
 def metric_of(workload):
     if is_selective(workload):
         return METRIC_SEL
+    if is_bwd(workload):
+        return METRIC_BWD
     return METRIC_DECODE if is_decode(workload) else METRIC
+
+
+def algorithmic_bwd(shape):
+    """Minimum HBM bytes of one backward pass: x, dt, B, C, dy (and init, dfinal) read once,
+    dx, ddt, dB, dC (and dinit) written once; A, D, dA, dD are negligible."""
+    b, L, H, P, N, G = (shape[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    e = 2 if shape["io_dtype"] == "bf16" else 4
+    st = b * H * P * N * 4
+    return 3 * b * L * H * P * e + 4 * b * L * G * N * e + 2 * b * L * H * 4 + 2 * st + (st if shape["init"] else 0)
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
 
 
@@ -232,6 +250,36 @@ def cpu_baseline_selective(inp, budget_s):
                       % (nch, D, b, L, reps, el)}
 
 
+def cpu_baseline_bwd(inp, dy, dfin, budget_s):
+    """The float64 adjoint oracle on the host over a bounded sample: whole sequences of as many
+    (batch 0) heads as fit the budget, tokens scaled to the layer."""
+    from oracle.ref_bwd import recurrence_bwd_np
+
+    b, L, H, P = inp.x.shape
+    G = inp.B.shape[2]
+    hpg = H // G
+
+    def run(nh):
+        sl = lambda a: np.ascontiguousarray(a[:1, :, :nh])
+        gsel = 1
+        t0 = time.perf_counter()
+        recurrence_bwd_np(sl(inp.x), np.ascontiguousarray(inp.dt[:1, :, :nh]), inp.A[:nh],
+                          np.ascontiguousarray(inp.B[:1, :, :gsel]), np.ascontiguousarray(inp.C[:1, :, :gsel]),
+                          inp.D[:nh], None if inp.init is None else np.ascontiguousarray(inp.init[:1, :nh]),
+                          np.ascontiguousarray(dy[:1, :, :nh]), np.ascontiguousarray(dfin[:1, :nh]))
+        return time.perf_counter() - t0
+
+    nh = min(2, H)   # two heads of group 0: the NumPy oracle's cost grows with heads x tokens
+    reps, el = 0, 0.0
+    while reps == 0 or (el < budget_s and reps < 100):
+        el += run(nh)
+        reps += 1
+    tokens = reps * L * nh / H   # whole-layer tokens of one sequence the sample amounts to
+    return {"value": tokens / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d heads of one sequence of %d tokens x %d passes, float64 adjoint "
+                      "recurrence (NumPy), %.1f s" % (nh, H, L, reps, el)}
+
+
 def cpu_baseline(inp, budget_s):
     """The float64 oracle as it stands, on the host cores, over a bounded sample of the
     workload: whole (batch, head) sequences, as many as fit the time budget."""
@@ -296,7 +344,16 @@ def run_reference(args):
         return
     from state_space_model_02_gb300 import synth
 
-    if is_selective(args.workload):
+    if is_bwd(args.workload):
+        base_wl = args.workload[len("bwd_"):]
+        inp = synth.make_config(base_wl, seed=args.seed)
+        shape = dict(synth.CONFIGS[base_wl])
+        rng = np.random.default_rng(args.seed + 1)
+        b_, L_, H_, P_ = inp.x.shape
+        dy_ = rng.standard_normal((b_, L_, H_, P_)).astype(np.float32)
+        df_ = rng.standard_normal((b_, H_, P_, inp.B.shape[3])).astype(np.float32)
+        baseline = lambda i, budget: cpu_baseline_bwd(i, dy_, df_, budget)
+    elif is_selective(args.workload):
         inp = synth.make_selective_config(args.workload, seed=args.seed)
         shape = dict(synth.SELECTIVE_CONFIGS[args.workload])
         baseline = cpu_baseline_selective
@@ -340,6 +397,8 @@ def run_ours(args):
 
     if is_selective(args.workload):
         return run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev)
+    if is_bwd(args.workload):
+        return run_bwd(args, torch, dist, ssd, synth, ws, rank, local, dev)
     shape = dict(synth.CONFIGS[args.workload])
     inp = synth.make_config(args.workload, seed=args.seed)
     bf16 = inp.io_dtype == "bf16"
@@ -506,6 +565,149 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def run_bwd(args, torch, dist, ssd, synth, ws, rank, local, dev):
+    """The backward arm: one ssd_bwd call per step (it runs the forward again inside)."""
+    base_wl = args.workload[len("bwd_"):]
+    shape = dict(synth.CONFIGS[base_wl])
+    inp = synth.make_config(base_wl, seed=args.seed)
+    bf16 = inp.io_dtype == "bf16"
+    rng = np.random.default_rng(args.seed + 1)
+    b, L, H, P = inp.x.shape
+    N = inp.B.shape[3]
+    dy_np = rng.standard_normal((b, L, H, P)).astype(np.float32)
+    df_np = rng.standard_normal((b, H, P, N)).astype(np.float32)
+    if bf16:
+        dy_np = synth.to_bf16_bits(dy_np)
+
+    def io(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else np.ascontiguousarray(a))
+        return t.view(torch.bfloat16) if bf16 else t
+
+    host = dict(x=io(inp.x), dt=torch.from_numpy(inp.dt), A=torch.from_numpy(inp.A), B=io(inp.B), C=io(inp.C),
+                D=torch.from_numpy(inp.D), init=None if inp.init is None else torch.from_numpy(inp.init),
+                dy=io(dy_np), dfin=torch.from_numpy(df_np))
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    prob = ssd.problem_of(d["x"], d["B"], inp.chunk)
+    wsbuf = torch.empty(ssd.load_library().ssd_bwd_workspace_bytes(ctypes_byref(prob)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(k):
+        flush.fill_(k & 0xFF)
+        flush_rd.max()
+
+    def step(src=d):
+        return ssd.bwd(src["x"], src["dt"], src["A"], src["B"], src["C"], src["D"], src["dy"], chunk=inp.chunk,
+                       init_state=src["init"], dfinal=src["dfin"], workspace=wsbuf, stream=stream)
+
+    for k in range(max(3, args.warmup)):
+        flush_l2(k)
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush_l2(k)
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    ms_step = max_over_ranks(ms_step, ws, dist, dev)
+    tokens = b * L
+    value = job_rate(tokens, ws, ms_step)
+    by = algorithmic_bwd(shape)
+    peaks = load_peaks()
+    ach = by / (ms_step * 1e-3) / 1e9
+    roofline = {"kernel": "ssd_bwd (whole pass)", "bound": "hbm", "achieved": ach, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": ach / peaks["hbm"], "traffic": None,
+                "peak_source": peaks["src"] + " (MEASURED_PEAKS.json burst)" if peaks["src"] == "measured" else "fallback"}
+
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in pin.items()}
+        outs_host = None
+        h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+
+        def e2e_step():
+            nonlocal outs_host
+            for k, v in pin.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            g = step(dev_in)
+            if outs_host is None:
+                outs_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in g.items() if v is not None}
+            for k, v in g.items():
+                if v is not None:
+                    outs_host[k].copy_(v, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dist, dev)
+        e2e = {"value": job_rate(tokens, ws, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        dyf = synth.bf16_bits_to_f32(dy_np) if bf16 else dy_np
+        cpu = cpu_baseline_bwd(inp, dyf, df_np, args.cpu_seconds)
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload; dy, dfinal ~ N(0, 1))",
+        "config": {"workload": args.workload, **shape,
+                   "l2": "flushed before every step (256 MiB write + 256 MiB read, outside the timed events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": roofline,
+        "kernels": {"ssd_bwd": {"us": 1e3 * ms_step, "share": 1.0, "alg_bytes": by}},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": bwd_launches(shape) * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def bwd_launches(shape):
+    """Kernel launches of one ssd_bwd call (dfinal given, dD and dinit wanted): two scans of 4
+    launches with their input copies and the scalar steps, then the role-swapped scan pairs,
+    one pair per 64-column slice when bf16 with headdim 64 (else one pair)."""
+    P, N = shape["headdim"], shape["dstate"]
+    init = 1 if shape["init"] else 0
+    kw = 64 if shape["io_dtype"] == "bf16" and P == 64 and N % 64 == 0 else N
+    head = 3 + 4 + 3 + 1 + 4 + 1 + 1 + 1 + 2 + init          # widen, scan, flips, decays, scan, combine, ...
+    per_slice = (1 + init + 4 + 1) + (1 + 1 + 4 + 1)
+    return head + 2 + (N // kw) * per_slice
+
+
+def ctypes_byref(prob):
+    import ctypes
+
+    return ctypes.byref(prob.c_shape())
 
 
 def run_selective(args, torch, dist, ssd, synth, ws, rank, local, dev):

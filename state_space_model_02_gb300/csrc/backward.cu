@@ -33,18 +33,18 @@ __device__ __forceinline__ void stf(uint16_t* p, int64_t i, float v) {
   p[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
-// dst[b, t, h, :] = src[b, flip ? L-1-t : t, h / rep, :], rows of `row_bytes` (a multiple of
-// 16) moved 16 bytes per thread
+// dst[b, t, h, :] = src[b, flip ? L-1-t : t, h / rep, v0 : v0 + vec_dst], in 16-byte vectors
+// (source rows of vec_src vectors, destination rows of vec_dst)
 __global__ void flip_expand_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t L,
-                                   int64_t Hsrc, int64_t Hdst, int64_t vec_per_row, bool flip,
-                                   int64_t total) {
+                                   int64_t Hsrc, int64_t Hdst, int64_t vec_src, int64_t vec_dst, int64_t v0,
+                                   bool flip, int64_t total) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
-  const int64_t v = i % vec_per_row, row = i / vec_per_row;
+  const int64_t v = i % vec_dst, row = i / vec_dst;
   const int64_t h = row % Hdst, bt = row / Hdst, t = bt % L, b = bt / L;
   const int64_t ts = flip ? L - 1 - t : t;
   const int64_t hs = h / (Hdst / Hsrc);
-  dst[i] = __ldg(src + ((b * L + ts) * Hsrc + hs) * vec_per_row + v);
+  dst[i] = __ldg(src + ((b * L + ts) * Hsrc + hs) * vec_src + v0 + v);
 }
 
 // float32 copy: dst[b, t, h, f] = src[b, flip ? L-1-t : t, h / rep, f], src float32 or bf16
@@ -69,43 +69,47 @@ __global__ void reverse_decay_kernel(const float* __restrict__ dt, float* __rest
   out[i] = t == 0 ? 0.f : __ldg(dt + (b * L + (L - t)) * H + h);
 }
 
-// (rows, P, N) -> (rows, N, P), float32
+// (rows, P, N) -> (rows, Nk, P) for the columns n0 .. n0 + Nk - 1, float32
 __global__ void transpose_state_kernel(const float* __restrict__ src, float* __restrict__ dst, int64_t P,
-                                       int64_t N, int64_t total) {
+                                       int64_t N, int64_t n0, int64_t Nk, int64_t total) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
-  const int64_t n = i % N, pr = i / N, p = pr % P, r = pr / P;
-  dst[(r * N + n) * P + p] = __ldg(src + i);
+  const int64_t n = i % Nk, pr = i / Nk, p = pr % P, r = pr / P;
+  dst[(r * Nk + n) * P + p] = __ldg(src + (r * P + p) * N + n0 + n);
 }
 
-// one warp per (b, t, h): dx, dL/dcs and <x, g B> from dy, x, y (without the skip term) and
-// the reverse scan's output g B (stored time-reversed)
+// one warp per (b, t, h): dx, dL/dcs, <x, g B> and <dy, x> from dy, x, y (without the skip
+// term) and the reverse scan's output g B (stored time-reversed)
 template <typename IO>
 __global__ void combine_kernel(const IO* __restrict__ dy, const IO* __restrict__ x, const float* __restrict__ yssm,
                                const float* __restrict__ gB_rev, const float* __restrict__ dt,
                                const float* __restrict__ D, IO* __restrict__ dx, float* __restrict__ dcs,
-                               float* __restrict__ xgB, int64_t L, int64_t H, int64_t P, int64_t rows) {
+                               float* __restrict__ xgB, float* __restrict__ dyx, int64_t L, int64_t H, int64_t P,
+                               int64_t rows) {
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int64_t h = row % H, bt = row / H, t = bt % L, b = bt / L;
   const int64_t rrow = (b * L + (L - 1 - t)) * H + h;
   const float d = __ldg(dt + row), dsk = D ? __ldg(D + h) : 0.f;
-  float s_dy = 0.f, s_xg = 0.f;
+  float s_dy = 0.f, s_xg = 0.f, s_dx = 0.f;
   for (int64_t p = lane; p < P; p += 32) {
     const float g = ldf(gB_rev, rrow * P + p), xv = ldf(x, row * P + p), dyv = ldf(dy, row * P + p);
     s_dy = fmaf(dyv, ldf(yssm, row * P + p), s_dy);
     s_xg = fmaf(xv, g, s_xg);
+    s_dx = fmaf(dyv, xv, s_dx);
     stf(dx, row * P + p, fmaf(d, g, dsk * dyv));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     s_dy += __shfl_xor_sync(0xffffffffu, s_dy, off);
     s_xg += __shfl_xor_sync(0xffffffffu, s_xg, off);
+    s_dx += __shfl_xor_sync(0xffffffffu, s_dx, off);
   }
   if (lane == 0) {
     dcs[row] = s_dy - d * s_xg;
     xgB[row] = s_xg;
+    dyx[row] = s_dx;
   }
 }
 
@@ -129,17 +133,19 @@ __global__ void final_dot_kernel(const float* __restrict__ dfinal, const float* 
 }
 
 // one warp per (b, h): the reverse cumulative sum r_t = sum_{s >= t} dL/dcs_s, in rounds of 32
-// tokens from the end; ddt_t = <x, g B>_t + A r_t and this (b, h)'s share of dA, sum dt_t r_t
+// tokens from the end; ddt_t = <x, g B>_t + A r_t, and this (b, h)'s shares of dA (sum dt_t r_t)
+// and of dD (sum <dy_t, x_t>)
 __global__ void reverse_cumsum_kernel(const float* __restrict__ dcs, const float* __restrict__ xgB,
-                                      const float* __restrict__ dt, const float* __restrict__ A,
-                                      float* __restrict__ ddt, float* __restrict__ dA_part, int64_t L,
+                                      const float* __restrict__ dyx, const float* __restrict__ dt,
+                                      const float* __restrict__ A, float* __restrict__ ddt,
+                                      float* __restrict__ dA_part, float* __restrict__ dD_part, int64_t L,
                                       int64_t H, int64_t BH) {
   const int64_t bh = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (bh >= BH) return;
   const int64_t b = bh / H, h = bh % H;
   const float a = __ldg(A + h);
-  float carry = 0.f, acc = 0.f;
+  float carry = 0.f, acc = 0.f, accd = 0.f;
   for (int64_t top = L - 1; top >= 0; top -= 32) {
     const int64_t t = top - lane;  // lane 0 takes the latest token of the round
     const int64_t i = (b * L + t) * H + h;
@@ -154,12 +160,19 @@ __global__ void reverse_cumsum_kernel(const float* __restrict__ dcs, const float
       const float d = __ldg(dt + i);
       ddt[i] = fmaf(a, r, __ldg(xgB + i));
       acc = fmaf(d, r, acc);
+      accd += __ldg(dyx + i);
     }
     carry += __shfl_sync(0xffffffffu, v, 31);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dA_part[bh] = acc;
+  for (int off = 16; off > 0; off >>= 1) {
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    accd += __shfl_xor_sync(0xffffffffu, accd, off);
+  }
+  if (lane == 0) {
+    dA_part[bh] = acc;
+    dD_part[bh] = accd;
+  }
 }
 
 // out[h] = sum_b part[b, h]
@@ -173,20 +186,22 @@ __global__ void sum_batches_kernel(const float* __restrict__ part, float* __rest
 
 // out[b, t, g, n] = sum over the heads h of group g of scale(b, t, h) y[b, t', h, n], with
 // t' = L-1-t when flip and scale = dt when given (else 1)
+// (y has Nk columns per row; out has N, of which n0 .. n0 + Nk - 1 are written)
 template <typename IO>
 __global__ void group_sum_kernel(const IO* __restrict__ y, const float* __restrict__ dt, IO* __restrict__ out,
-                                 int64_t L, int64_t H, int64_t G, int64_t N, bool flip, int64_t total) {
+                                 int64_t L, int64_t H, int64_t G, int64_t N, int64_t n0, int64_t Nk, bool flip,
+                                 int64_t total) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
-  const int64_t n = i % N, r = i / N, g = r % G, bt = r / G, t = bt % L, b = bt / L;
+  const int64_t n = i % Nk, r = i / Nk, g = r % G, bt = r / G, t = bt % L, b = bt / L;
   const int64_t hpg = H / G, ts = flip ? L - 1 - t : t;
   float s = 0.f;
   for (int64_t k = 0; k < hpg; ++k) {
     const int64_t h = g * hpg + k;
     const float sc = dt ? __ldg(dt + (b * L + t) * H + h) : 1.f;
-    s = fmaf(sc, ldf(y, ((b * L + ts) * H + h) * N + n), s);
+    s = fmaf(sc, ldf(y, ((b * L + ts) * H + h) * Nk + n), s);
   }
-  stf(out, i, s);
+  stf(out, r * N + n0 + n, s);
 }
 
 // dinit = a_0 g_0 = exp(A dt_0) times the reverse scan's final state
@@ -198,38 +213,17 @@ __global__ void dinit_kernel(const float* __restrict__ g0, const float* __restri
   dinit[i] = expf(__ldg(A + h) * __ldg(dt + (b * L) * H + h)) * __ldg(g0 + i);
 }
 
-// one block per head: dD[h] = sum over (b, t, p) of dy x
-template <typename IO>
-__global__ void dD_kernel(const IO* __restrict__ dy, const IO* __restrict__ x, float* __restrict__ dD, int64_t BL,
-                          int64_t H, int64_t P) {
-  __shared__ float red[32];
-  const int64_t h = blockIdx.x;
-  float s = 0.f;
-  for (int64_t i = threadIdx.x; i < BL * P; i += blockDim.x) {
-    const int64_t bt = i / P, p = i % P, e = (bt * H + h) * P + p;
-    s = fmaf(ldf(dy, e), ldf(x, e), s);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = s;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    s = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (threadIdx.x == 0) dD[h] = s;
-  }
-}
-
 inline unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n + per - 1) / per); }
 
 }  // namespace
 
 cudaError_t launch_flip_expand(const void* src, void* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
-                               int64_t row_bytes, bool flip, cudaStream_t st) {
-  const int64_t vpr = row_bytes / 16, total = b * L * Hdst * vpr;
+                               int64_t src_row_bytes, int64_t col_byte0, int64_t dst_row_bytes, bool flip,
+                               cudaStream_t st) {
+  const int64_t total = b * L * Hdst * (dst_row_bytes / 16);
   flip_expand_kernel<<<blocks_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                             L, Hsrc, Hdst, vpr, flip, total);
+                                                             L, Hsrc, Hdst, src_row_bytes / 16, dst_row_bytes / 16,
+                                                             col_byte0 / 16, flip, total);
   return cudaGetLastError();
 }
 
@@ -239,23 +233,26 @@ cudaError_t launch_reverse_decay(const float* dt, float* out, int64_t b, int64_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_state(const float* src, float* dst, int64_t rows, int64_t P, int64_t N, cudaStream_t st) {
-  const int64_t total = rows * P * N;
-  transpose_state_kernel<<<blocks_for(total, 256), 256, 0, st>>>(src, dst, P, N, total);
+cudaError_t launch_transpose_state(const float* src, float* dst, int64_t rows, int64_t P, int64_t N, int64_t n0,
+                                   int64_t Nk, cudaStream_t st) {
+  const int64_t total = rows * P * Nk;
+  transpose_state_kernel<<<blocks_for(total, 256), 256, 0, st>>>(src, dst, P, N, n0, Nk, total);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_combine(const Problem& p, const void* dy, const void* x, const float* yssm, const float* gB_rev,
-                               const float* dt, const float* D, void* dx, float* dcs, float* xgB, cudaStream_t st) {
+                               const float* dt, const float* D, void* dx, float* dcs, float* xgB, float* dyx,
+                               cudaStream_t st) {
   const int64_t rows = p.b * p.L * p.H;
   const unsigned grid = blocks_for(rows, 8);
   if (p.io_bf16)
     combine_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(x),
-                                                   yssm, gB_rev, dt, D, static_cast<uint16_t*>(dx), dcs, xgB, p.L,
-                                                   p.H, p.P, rows);
+                                                   yssm, gB_rev, dt, D, static_cast<uint16_t*>(dx), dcs, xgB, dyx,
+                                                   p.L, p.H, p.P, rows);
   else
     combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(dy), static_cast<const float*>(x), yssm,
-                                                gB_rev, dt, D, static_cast<float*>(dx), dcs, xgB, p.L, p.H, p.P, rows);
+                                                gB_rev, dt, D, static_cast<float*>(dx), dcs, xgB, dyx, p.L, p.H,
+                                                p.P, rows);
   return cudaGetLastError();
 }
 
@@ -272,24 +269,25 @@ cudaError_t launch_widen_flip_expand(const void* src, float* dst, int64_t b, int
 }
 
 cudaError_t launch_bwd_scalars(const Problem& p, const float* dfinal, const float* fin, const float* xgB,
-                               const float* dt, const float* A, float* dcs, float* ddt, float* dA_part, float* dA,
-                               cudaStream_t st) {
+                               const float* dyx, const float* dt, const float* A, float* dcs, float* ddt,
+                               float* part, float* dA, float* dD, cudaStream_t st) {
   if (dfinal) final_dot_kernel<<<static_cast<unsigned>(p.b * p.H), 256, 0, st>>>(dfinal, fin, dcs, p.L, p.H, p.P * p.N);
   const int64_t BH = p.b * p.H;
-  reverse_cumsum_kernel<<<blocks_for(BH, 8), 256, 0, st>>>(dcs, xgB, dt, A, ddt, dA_part, p.L, p.H, BH);
-  sum_batches_kernel<<<blocks_for(p.H, 128), 128, 0, st>>>(dA_part, dA, p.b, p.H);
+  reverse_cumsum_kernel<<<blocks_for(BH, 8), 256, 0, st>>>(dcs, xgB, dyx, dt, A, ddt, part, part + BH, p.L, p.H, BH);
+  sum_batches_kernel<<<blocks_for(p.H, 128), 128, 0, st>>>(part, dA, p.b, p.H);
+  if (dD) sum_batches_kernel<<<blocks_for(p.H, 128), 128, 0, st>>>(part + BH, dD, p.b, p.H);
   return cudaGetLastError();
 }
 
-cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t N, bool flip,
-                             cudaStream_t st) {
-  const int64_t total = p.b * p.L * p.G * N;
+cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t n0, int64_t Nk,
+                             bool flip, cudaStream_t st) {
+  const int64_t total = p.b * p.L * p.G * Nk;
   if (p.io_bf16)
     group_sum_kernel<uint16_t><<<blocks_for(total, 256), 256, 0, st>>>(
-        static_cast<const uint16_t*>(y), dt, static_cast<uint16_t*>(out), p.L, p.H, p.G, N, flip, total);
+        static_cast<const uint16_t*>(y), dt, static_cast<uint16_t*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip, total);
   else
     group_sum_kernel<float><<<blocks_for(total, 256), 256, 0, st>>>(
-        static_cast<const float*>(y), dt, static_cast<float*>(out), p.L, p.H, p.G, N, flip, total);
+        static_cast<const float*>(y), dt, static_cast<float*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip, total);
   return cudaGetLastError();
 }
 
@@ -297,16 +295,6 @@ cudaError_t launch_dinit(const Problem& p, const float* g0, const float* dt, con
                          cudaStream_t st) {
   const int64_t total = p.b * p.H * p.P * p.N;
   dinit_kernel<<<blocks_for(total, 256), 256, 0, st>>>(g0, dt, A, dinit, p.L, p.H, p.P * p.N, total);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dD(const Problem& p, const void* dy, const void* x, float* dD, cudaStream_t st) {
-  if (p.io_bf16)
-    dD_kernel<uint16_t><<<static_cast<unsigned>(p.H), 512, 0, st>>>(static_cast<const uint16_t*>(dy),
-                                                                     static_cast<const uint16_t*>(x), dD, p.b * p.L, p.H, p.P);
-  else
-    dD_kernel<float><<<static_cast<unsigned>(p.H), 512, 0, st>>>(static_cast<const float*>(dy),
-                                                                  static_cast<const float*>(x), dD, p.b * p.L, p.H, p.P);
   return cudaGetLastError();
 }
 

@@ -394,16 +394,22 @@ namespace {
 
 // Regions of the backward workspace (each 256-byte aligned).
 struct BwdLayout {
-  size_t scan, y, fin, xin, bin, cin, dtr, init, out, fin1, dcs, xgb, dap, total;
+  size_t scan, y, fin, xin, bin, cin, dtr, init, out, fin1, dcs, xgb, dyx, part, total;
 };
 
-// The transposed problem of the two role-swapped scans: head dim N, state P, one group per head.
+// The role-swapped scans (dC, dB) have head dim N and state P with one group per head.  They
+// are linear in their x input, so they run as N / kSplit scans of head dim kSplit, a
+// tensor-core shape, when P is 64 with bf16 I/O (else as one scan of head dim N).
+constexpr int64_t kSplit = 64;
+int64_t swapped_width(const ssd_shape& s) {
+  return (s.io_dtype == SSD_BF16 && s.headdim == 64 && s.dstate % kSplit == 0) ? kSplit : s.dstate;
+}
 ssd_shape swapped_shape(const ssd_shape& s) {
   ssd_shape t = s;
-  t.headdim = s.dstate;
+  t.headdim = swapped_width(s);
   t.dstate = s.headdim;
   t.ngroups = s.nheads;
-  t.flags = 0;
+  t.flags = s.flags;
   return t;
 }
 
@@ -433,7 +439,8 @@ bool bwd_layout(const ssd_shape* shape, BwdLayout* l) {
   l->fin1 = take(size_t(p.b * p.H) * PN * 4);
   l->dcs = take(BL * p.H * 4);
   l->xgb = take(BL * p.H * 4);
-  l->dap = take(size_t(p.b * p.H) * 4);
+  l->dyx = take(BL * p.H * 4);
+  l->part = take(size_t(p.b * p.H) * 8);
   l->total = o;
   return true;
 }
@@ -502,7 +509,8 @@ ssd_status ssd_bwd(const ssd_shape* shape, const void* x, const float* dt, const
   float* t_fin1 = reinterpret_cast<float*>(w + l.fin1);
   float* t_dcs = reinterpret_cast<float*>(w + l.dcs);
   float* t_xgb = reinterpret_cast<float*>(w + l.xgb);
-  float* t_dap = reinterpret_cast<float*>(w + l.dap);
+  float* t_dyx = reinterpret_cast<float*>(w + l.dyx);
+  float* t_part = reinterpret_cast<float*>(w + l.part);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t e = p.io_bf16 ? 2 : 4;
   const bool bf = p.io_bf16;
@@ -529,23 +537,30 @@ ssd_status ssd_bwd(const ssd_shape* shape, const void* x, const float* dt, const
   SSD_TRY(cuda_ok(ssd::launch_reverse_decay(dt, t_dtr, p.b, p.L, p.H, st), "reverse decay"));
   SSD_TRY(run_scan(pf, ws_scan, fx, t_dtr, A, fb, fc, dfinal, fo, t_fin1, true, st));
   // 3. dx, dL/dcs, ddt, dA, dD, dinit
-  SSD_TRY(cuda_ok(ssd::launch_bwd_combine(p, dy, x, fy, fo, dt, D, dx, t_dcs, t_xgb, st), "combine"));
-  SSD_TRY(cuda_ok(ssd::launch_bwd_scalars(p, dfinal, t_fin, t_xgb, dt, A, t_dcs, ddt, t_dap, dA, st), "scalars"));
+  SSD_TRY(cuda_ok(ssd::launch_bwd_combine(p, dy, x, fy, fo, dt, D, dx, t_dcs, t_xgb, t_dyx, st), "combine"));
+  SSD_TRY(cuda_ok(ssd::launch_bwd_scalars(p, dfinal, t_fin, t_xgb, t_dyx, dt, A, t_dcs, ddt, t_part, dA, dD, st),
+                  "scalars"));
   if (dinit) SSD_TRY(cuda_ok(ssd::launch_dinit(p, t_fin1, dt, A, dinit, st), "dinit"));
-  if (dD) SSD_TRY(cuda_ok(ssd::launch_dD(p, dy, x, dD, st), "dD"));
-  // 4. dC: forward scan with x <- B (per head), B <- x, C <- dy, from init^T; summed per group
-  SSD_TRY(cuda_ok(ssd::launch_flip_expand(B, t_x, p.b, p.L, p.G, p.H, p.N * e, false, st), "expand"));
-  if (init_state) SSD_TRY(cuda_ok(ssd::launch_transpose_state(init_state, t_init, p.b * p.H, p.P, p.N, st), "transpose"));
-  SSD_TRY(run_scan(q, ws_scan, t_x, dt, A, x, dy, init_state ? t_init : nullptr, t_out, nullptr, false, st));
-  SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, nullptr, dC, p.N, false, st), "group sum"));
-  // 5. dB: reversed scan with x <- C (per head), B <- dy, C <- x, from dfinal^T; times dt,
+  // 4. dC: forward scans with x <- B (per head, kw columns at a time), B <- x, C <- dy, from
+  //    init^T; summed per group into those columns of dC
+  // 5. dB: reversed scans with x <- C (per head), B <- dy, C <- x, from dfinal^T; times dt,
   //    summed per group
-  SSD_TRY(cuda_ok(ssd::launch_flip_expand(C, t_x, p.b, p.L, p.G, p.H, p.N * e, true, st), "flip"));
-  SSD_TRY(cuda_ok(ssd::launch_flip_expand(dy, t_b, p.b, p.L, p.H, p.H, p.P * e, true, st), "flip"));
-  SSD_TRY(cuda_ok(ssd::launch_flip_expand(x, t_c, p.b, p.L, p.H, p.H, p.P * e, true, st), "flip"));
-  if (dfinal) SSD_TRY(cuda_ok(ssd::launch_transpose_state(dfinal, t_init, p.b * p.H, p.P, p.N, st), "transpose"));
-  SSD_TRY(run_scan(q, ws_scan, t_x, t_dtr, A, t_b, t_c, dfinal ? t_init : nullptr, t_out, nullptr, true, st));
-  SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, dt, dB, p.N, true, st), "group sum"));
+  const int64_t kw = q.P;
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(dy, t_b, p.b, p.L, p.H, p.H, p.P * e, 0, p.P * e, true, st), "flip"));
+  SSD_TRY(cuda_ok(ssd::launch_flip_expand(x, t_c, p.b, p.L, p.H, p.H, p.P * e, 0, p.P * e, true, st), "flip"));
+  for (int64_t n0 = 0; n0 < p.N; n0 += kw) {
+    SSD_TRY(cuda_ok(ssd::launch_flip_expand(B, t_x, p.b, p.L, p.G, p.H, p.N * e, n0 * e, kw * e, false, st), "expand"));
+    if (init_state)
+      SSD_TRY(cuda_ok(ssd::launch_transpose_state(init_state, t_init, p.b * p.H, p.P, p.N, n0, kw, st), "transpose"));
+    SSD_TRY(run_scan(q, ws_scan, t_x, dt, A, x, dy, init_state ? t_init : nullptr, t_out, nullptr, false, st));
+    SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, nullptr, dC, n0, kw, false, st), "group sum"));
+
+    SSD_TRY(cuda_ok(ssd::launch_flip_expand(C, t_x, p.b, p.L, p.G, p.H, p.N * e, n0 * e, kw * e, true, st), "flip"));
+    if (dfinal)
+      SSD_TRY(cuda_ok(ssd::launch_transpose_state(dfinal, t_init, p.b * p.H, p.P, p.N, n0, kw, st), "transpose"));
+    SSD_TRY(run_scan(q, ws_scan, t_x, t_dtr, A, t_b, t_c, dfinal ? t_init : nullptr, t_out, nullptr, true, st));
+    SSD_TRY(cuda_ok(ssd::launch_group_sum(p, t_out, dt, dB, n0, kw, true, st), "group sum"));
+  }
   g_last_error[0] = '\0';
   return SSD_OK;
 }

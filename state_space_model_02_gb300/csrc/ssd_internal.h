@@ -84,21 +84,23 @@ cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* 
 
 // Backward pass: the steps between its scans (backward.cu).
 cudaError_t launch_flip_expand(const void* src, void* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
-                               int64_t row_bytes, bool flip, cudaStream_t st);
-cudaError_t launch_reverse_decay(const float* dt, float* out, int64_t b, int64_t L, int64_t H, cudaStream_t st);
-cudaError_t launch_transpose_state(const float* src, float* dst, int64_t rows, int64_t P, int64_t N, cudaStream_t st);
+                               int64_t src_row_bytes, int64_t col_byte0, int64_t dst_row_bytes, bool flip,
+                               cudaStream_t st);
 cudaError_t launch_widen_flip_expand(const void* src, float* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
                                      int64_t F, bool flip, bool src_bf16, cudaStream_t st);
+cudaError_t launch_reverse_decay(const float* dt, float* out, int64_t b, int64_t L, int64_t H, cudaStream_t st);
+cudaError_t launch_transpose_state(const float* src, float* dst, int64_t rows, int64_t P, int64_t N, int64_t n0,
+                                   int64_t Nk, cudaStream_t st);
 cudaError_t launch_bwd_combine(const Problem& p, const void* dy, const void* x, const float* yssm, const float* gB_rev,
-                               const float* dt, const float* D, void* dx, float* dcs, float* xgB, cudaStream_t st);
-cudaError_t launch_bwd_scalars(const Problem& p, const float* dfinal, const float* fin, const float* xgB,
-                               const float* dt, const float* A, float* dcs, float* ddt, float* dA_part, float* dA,
+                               const float* dt, const float* D, void* dx, float* dcs, float* xgB, float* dyx,
                                cudaStream_t st);
-cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t N, bool flip,
-                             cudaStream_t st);
+cudaError_t launch_bwd_scalars(const Problem& p, const float* dfinal, const float* fin, const float* xgB,
+                               const float* dyx, const float* dt, const float* A, float* dcs, float* ddt,
+                               float* part, float* dA, float* dD, cudaStream_t st);
+cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t n0, int64_t Nk,
+                             bool flip, cudaStream_t st);
 cudaError_t launch_dinit(const Problem& p, const float* g0, const float* dt, const float* A, float* dinit,
                          cudaStream_t st);
-cudaError_t launch_dD(const Problem& p, const void* dy, const void* x, float* dD, cudaStream_t st);
 
 // Mamba-1 selective scan (fused zero-order hold + scan + read-out); applicability by selective_ok.
 bool selective_ok(const SelProblem& p);
