@@ -404,6 +404,16 @@ constexpr int64_t kSplit = 64;
 int64_t swapped_width(const ssd_shape& s) {
   return (s.io_dtype == SSD_BF16 && s.headdim == 64 && s.dstate % kSplit == 0) ? kSplit : s.dstate;
 }
+// The two scans that run in float32 (the forward again and the adjoint scan) take the
+// CUDA-core kernels, whose in-chunk (quadratic) work grows with the chunk length: they use
+// 64-token chunks whatever the forward's chunk (same arithmetic, a different blocking).
+ssd_shape f32_shape(const ssd_shape& s) {
+  ssd_shape t = s;
+  t.io_dtype = SSD_F32;
+  t.chunk = 64;
+  return t;
+}
+
 ssd_shape swapped_shape(const ssd_shape& s) {
   ssd_shape t = s;
   t.headdim = swapped_width(s);
@@ -418,8 +428,9 @@ bool bwd_layout(const ssd_shape* shape, BwdLayout* l) {
   if (make_problem(shape, &p) != SSD_OK) return false;
   const ssd_shape sw = swapped_shape(*shape);
   if (make_problem(&sw, &q) != SSD_OK) return false;
-  ssd::Problem pf = p;  // the float32 scans
-  pf.io_bf16 = false;
+  ssd::Problem pf;      // the float32 scans
+  const ssd_shape fs = f32_shape(*shape);
+  if (make_problem(&fs, &pf) != SSD_OK) return false;
   const size_t e = 4;   // every scan buffer is sized for float32
   const size_t BL = size_t(p.b * p.L), PN = size_t(p.P * p.N);
   const size_t F = size_t(p.P > p.N ? p.P : p.N);
@@ -514,8 +525,9 @@ ssd_status ssd_bwd(const ssd_shape* shape, const void* x, const float* dt, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t e = p.io_bf16 ? 2 : 4;
   const bool bf = p.io_bf16;
-  ssd::Problem pf = p;
-  pf.io_bf16 = false;
+  ssd::Problem pf;
+  const ssd_shape fs = f32_shape(*shape);
+  SSD_TRY(make_problem(&fs, &pf));
   float* fx = static_cast<float*>(t_x);
   float* fb = static_cast<float*>(t_b);
   float* fc = static_cast<float*>(t_c);
