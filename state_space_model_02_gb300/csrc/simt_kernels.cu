@@ -27,154 +27,179 @@ __device__ __forceinline__ void st_io(uint16_t* p, int64_t i, float v) {
   p[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
-constexpr int T = 32;  // tile edge
+// Both kernels are tiled matrix products on 64 x 64 output tiles: 256 threads, thread
+// (tx, ty) = (tid % 16, tid / 16) owns rows 4 ty .. 4 ty + 3 and columns 4 tx .. 4 tx + 3, and
+// every k step reads one float4 of each operand from shared memory (operands staged k-major,
+// 16 k values at a time) for 16 fused multiply-adds.
+constexpr int TM = 64;  // tile edge
+constexpr int KT = 16;  // k values staged per step
+constexpr int GS = TM + 4;  // row stride of the masked-matrix buffer (keeps float4 alignment)
 
-// grid: x = p-tile * n_tiles + n-tile, y = h, z = b * nc + c.  256 threads, 32x32 outputs.
+__device__ __forceinline__ void mma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
+  const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+}
+
+// grid: x = p-tile * n_tiles + n-tile, y = h, z = b * nc + c.  S tile (64 p x 64 n) =
+// sum over the chunk's tokens t of (w_t x[t, p]) B[t, n].
 template <typename IO>
 __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const float* __restrict__ cs2,
     const float* __restrict__ dtT, IO* __restrict__ S, int64_t L, int64_t H, int64_t P,
     int64_t N, int64_t G, int64_t Q, int64_t nc) {
-  __shared__ float xs[T][T + 1];
-  __shared__ float bs[T][T + 1];
-  const int tid = threadIdx.x, tx = tid % T, ty = tid / T;  // ty in 0..7
-  const int64_t n_tiles = (N + T - 1) / T;
-  const int64_t p0 = (blockIdx.x / n_tiles) * T, n0 = (blockIdx.x % n_tiles) * T;
+  __shared__ __align__(16) float As[KT][TM];  // As[k][p] = w x[t0 + k, p0 + p]
+  __shared__ __align__(16) float Bs[KT][TM];  // Bs[k][n] = B[t0 + k, n0 + n]
+  __shared__ float wsm[KT];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t n_tiles = (N + TM - 1) / TM;
+  const int64_t p0 = (blockIdx.x / n_tiles) * TM, n0 = (blockIdx.x % n_tiles) * TM;
   const int64_t h = blockIdx.y, bc = blockIdx.z, b = bc / nc, c = bc % nc;
   const int64_t g = h / (H / G);
   const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
   const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
   const float last = csr[Q - 1];
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t t0 = 0; t0 < Q; t0 += T) {
-    // xs[t][p] = w_t * x[t, p], bs[t][n] = B[t, n]
-    for (int e = tid; e < T * T; e += 256) {
-      const int tt = e / T, cc = e % T;
-      const int64_t t = t0 + tt, tok = c * Q + t;
-      float xv = 0.f, bv = 0.f;
-      if (tok < L) {
-        const float w = ex2(last - csr[t]) * dtr[t];
-        if (p0 + cc < P) xv = w * ld_io(x, ((b * L + tok) * H + h) * P + p0 + cc);
-        if (n0 + cc < N) bv = ld_io(Bm, ((b * L + tok) * G + g) * N + n0 + cc);
-      }
-      xs[tt][cc] = xv;
-      bs[tt][cc] = bv;
+  float acc[4][4] = {};
+  for (int64_t t0 = 0; t0 < Q; t0 += KT) {
+    if (tid < KT) {
+      const int64_t tok = c * Q + t0 + tid;
+      wsm[tid] = tok < L ? ex2(last - csr[t0 + tid]) * dtr[t0 + tid] : 0.f;
     }
     __syncthreads();
-#pragma unroll 8
-    for (int tt = 0; tt < T; ++tt) {
-      const float bv = bs[tt][tx];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = fmaf(xs[tt][ty + 8 * k], bv, acc[k]);
+    for (int e = tid; e < KT * TM; e += 256) {
+      const int k = e / TM, col = e % TM;
+      const int64_t tok = c * Q + t0 + k;
+      float xv = 0.f, bv = 0.f;
+      if (tok < L) {
+        if (p0 + col < P) xv = wsm[k] * ld_io(x, ((b * L + tok) * H + h) * P + p0 + col);
+        if (n0 + col < N) bv = ld_io(Bm, ((b * L + tok) * G + g) * N + n0 + col);
+      }
+      As[k][col] = xv;
+      Bs[k][col] = bv;
     }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < KT; ++k)
+      mma4x4(acc, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
     __syncthreads();
   }
   IO* out = S + (((b * nc + c) * H + h) * P) * N;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t p = p0 + ty + 8 * k, n = n0 + tx;
-    if (p < P && n < N) st_io(out, p * N + n, acc[k]);
-  }
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int64_t p = p0 + 4 * ty + r, n = n0 + 4 * tx + cc;
+      if (p < P && n < N) st_io(out, p * N + n, acc[r][cc]);
+    }
 }
 
-// grid: x = row tile (32 rows of the chunk), y = h, z = b * nc + c.  256 threads.
-// Dynamic shared memory: Gs[32][Q] (masked, decayed C.B^T rows).
+// grid: x = 64-row tile of the chunk, y = h, z = b * nc + c; dynamic shared memory holds the
+// masked matrix of the tile's rows, transposed: GsT[j][i] = 2^{cs2_i - cs2_j} dt_j (C_i . B_j)
+// for j <= i (0 above the diagonal), j < jmax.
 template <typename IO, typename HT>
 __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const IO* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ cs2, const float* __restrict__ dtT,
     const HT* __restrict__ hprev, IO* __restrict__ y, int64_t L, int64_t H, int64_t P, int64_t N,
     int64_t G, int64_t Q, int64_t nc) {
-  extern __shared__ float Gs[];  // [T][Q]
-  __shared__ float cs_s[T], e_s[T];
-  __shared__ float ta[T][T + 1];
-  __shared__ float tb[T][T + 1];
-  const int tid = threadIdx.x, tx = tid % T, ty = tid / T;
-  const int64_t i0 = int64_t(blockIdx.x) * T;
+  extern __shared__ __align__(16) float GsT[];  // [jmax][GS]
+  __shared__ __align__(16) float As[KT][TM];
+  __shared__ __align__(16) float Bs[KT][TM];
+  __shared__ float cs_i[TM], e_i[TM];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t i0 = int64_t(blockIdx.x) * TM;
   const int64_t h = blockIdx.y, bc = blockIdx.z, b = bc / nc, c = bc % nc;
   const int64_t g = h / (H / G);
   const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
   const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
-  const int64_t jmax = i0 + T;  // columns j < jmax can be causal for these rows
-  if (tid < T) {
-    cs_s[tid] = csr[i0 + tid];
-    e_s[tid] = ex2(csr[i0 + tid]);
+  const int64_t jmax = i0 + TM < Q ? i0 + TM : Q;  // columns j < jmax can be causal for these rows
+  if (tid < TM) {
+    const bool in = i0 + tid < Q;
+    cs_i[tid] = in ? csr[i0 + tid] : 0.f;
+    e_i[tid] = in ? ex2(csr[i0 + tid]) : 0.f;
   }
+  auto row_ok = [&](int64_t i_chunk) { return i_chunk < Q && c * Q + i_chunk < L; };
 
-  // Phase 1: Gs[i][j] = C_i . B_j for rows i0..i0+31 and j < jmax, then mask and decay.
-  for (int64_t j0 = 0; j0 < jmax; j0 += T) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t n0 = 0; n0 < N; n0 += T) {
-      for (int e = tid; e < T * T; e += 256) {
-        const int r = e / T, cc = e % T;
-        const int64_t ti = c * Q + i0 + r, tj = c * Q + j0 + r, n = n0 + cc;
-        ta[r][cc] = (ti < L && n < N) ? ld_io(Cm, ((b * L + ti) * G + g) * N + n) : 0.f;
-        tb[r][cc] = (tj < L && n < N) ? ld_io(Bm, ((b * L + tj) * G + g) * N + n) : 0.f;
+  // Phase 1: C_i . B_j over n, masked and decayed, into GsT
+  for (int64_t j0 = 0; j0 < jmax; j0 += TM) {
+    float acc[4][4] = {};
+    for (int64_t n0 = 0; n0 < N; n0 += KT) {
+      for (int e = tid; e < KT * TM; e += 256) {
+        const int r = e / KT, k = e % KT;  // consecutive threads read consecutive n
+        const int64_t n = n0 + k;
+        const int64_t ti = i0 + r, tj = j0 + r;
+        As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
+        Bs[k][r] = (row_ok(tj) && n < N) ? ld_io(Bm, ((b * L + c * Q + tj) * G + g) * N + n) : 0.f;
       }
       __syncthreads();
-#pragma unroll 8
-      for (int nn = 0; nn < T; ++nn) {
-        const float bv = tb[tx][nn];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = fmaf(ta[ty + 8 * k][nn], bv, acc[k]);
-      }
+      for (int k = 0; k < KT; ++k)
+        mma4x4(acc, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
       __syncthreads();
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int il = ty + 8 * k;
-      const int64_t i = i0 + il, j = j0 + tx;
-      float v = 0.f;
-      if (j <= i) v = acc[k] * ex2(cs_s[il] - csr[j]) * dtr[j];
-      Gs[il * Q + j] = v;
+    for (int cc = 0; cc < 4; ++cc) {
+      const int64_t j = j0 + 4 * tx + cc;
+      if (j >= jmax) continue;
+      const float cj = j < Q ? csr[j] : 0.f, dj = j < Q ? dtr[j] : 0.f;
+      float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int il = 4 * ty + r;
+        v[r] = (j <= i0 + il) ? acc[r][cc] * ex2(cs_i[il] - cj) * dj : 0.f;
+      }
+      *reinterpret_cast<float4*>(&GsT[j * GS + 4 * ty]) = make_float4(v[0], v[1], v[2], v[3]);
     }
   }
   __syncthreads();
 
-  // Phase 2: y[i][p] for p tiles of 32.
+  // Phase 2, per 64-column tile of p: y = GsT^T x + 2^{cs2_i} C hprev^T + D x
   const float Dh = D ? D[h] : 0.f;
-  for (int64_t p0 = 0; p0 < P; p0 += T) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t j0 = 0; j0 < jmax; j0 += T) {
-      for (int e = tid; e < T * T; e += 256) {
-        const int r = e / T, cc = e % T;
-        const int64_t tj = c * Q + j0 + r;
-        ta[r][cc] = (tj < L && p0 + cc < P) ? ld_io(x, ((b * L + tj) * H + h) * P + p0 + cc) : 0.f;
+  const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
+  for (int64_t p0 = 0; p0 < P; p0 += TM) {
+    float acc1[4][4] = {}, acc2[4][4] = {};
+    for (int64_t k0 = 0; k0 < jmax; k0 += KT) {
+      for (int e = tid; e < KT * TM; e += 256) {
+        const int k = e / TM, col = e % TM;
+        const int64_t tj = k0 + k;
+        Bs[k][col] = (tj < jmax && row_ok(tj) && p0 + col < P) ? ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) : 0.f;
       }
       __syncthreads();
-#pragma unroll 8
-      for (int jj = 0; jj < T; ++jj) {
-        const float xv = ta[jj][tx];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = fmaf(Gs[(ty + 8 * k) * Q + j0 + jj], xv, acc[k]);
+      for (int k = 0; k < KT; ++k) {
+        if (k0 + k < jmax)
+          mma4x4(acc1, *reinterpret_cast<const float4*>(&GsT[(k0 + k) * GS + 4 * ty]),
+                 *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
       }
       __syncthreads();
     }
-    const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
-    for (int64_t n0 = 0; n0 < N; n0 += T) {
-      for (int e = tid; e < T * T; e += 256) {
-        const int r = e / T, cc = e % T;
-        const int64_t ti = c * Q + i0 + r, n = n0 + cc;
-        ta[r][cc] = (ti < L && n < N) ? ld_io(Cm, ((b * L + ti) * G + g) * N + n) : 0.f;
-        tb[r][cc] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
+    for (int64_t n0 = 0; n0 < N; n0 += KT) {
+      for (int e = tid; e < KT * TM; e += 256) {
+        const int r = e / KT, k = e % KT;
+        const int64_t n = n0 + k, ti = i0 + r;
+        As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
+        Bs[k][r] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
       }
       __syncthreads();
-#pragma unroll 8
-      for (int nn = 0; nn < T; ++nn) {
-        const float hv = tb[tx][nn];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc2[k] = fmaf(ta[ty + 8 * k][nn], hv, acc2[k]);
-      }
+      for (int k = 0; k < KT; ++k)
+        mma4x4(acc2, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
       __syncthreads();
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int il = ty + 8 * k;
-      const int64_t ti = c * Q + i0 + il, p = p0 + tx;
-      if (ti < L && p < P) {
-        const int64_t off = ((b * L + ti) * H + h) * P + p;
-        st_io(y, off, acc[k] + e_s[il] * acc2[k] + Dh * ld_io(x, off));
+    for (int r = 0; r < 4; ++r) {
+      const int il = 4 * ty + r;
+      const int64_t ti = i0 + il;
+      if (!row_ok(ti)) continue;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int64_t p = p0 + 4 * tx + cc;
+        if (p < P) {
+          const int64_t off = ((b * L + c * Q + ti) * H + h) * P + p;
+          st_io(y, off, acc1[r][cc] + e_i[il] * acc2[r][cc] + Dh * ld_io(x, off));
+        }
       }
     }
   }
@@ -184,7 +209,7 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
 
 cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void* B, const float* cs2,
                                     const float* dtT, void* S, cudaStream_t st) {
-  const int64_t tiles = ((p.P + T - 1) / T) * ((p.N + T - 1) / T);
+  const int64_t tiles = ((p.P + TM - 1) / TM) * ((p.N + TM - 1) / TM);
   const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.H),
                   static_cast<unsigned>(p.b * p.nc));
   if (p.io_bf16)
@@ -202,17 +227,22 @@ cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void*
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(p.Q / T), static_cast<unsigned>(p.H),
+  const dim3 grid(static_cast<unsigned>((p.Q + TM - 1) / TM), static_cast<unsigned>(p.H),
                   static_cast<unsigned>(p.b * p.nc));
-  const size_t smem = static_cast<size_t>(T) * p.Q * sizeof(float);
+  const size_t smem = static_cast<size_t>(p.Q) * GS * sizeof(float);
+  cudaError_t e;
   if (p.io_bf16) {
     auto k = chunk_scan_simt_kernel<uint16_t, uint16_t>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     k<<<grid, 256, smem, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(B),
                                static_cast<const uint16_t*>(C), D, cs2, dtT,
                                static_cast<const uint16_t*>(hprev), static_cast<uint16_t*>(y), p.L,
                                p.H, p.P, p.N, p.G, p.Q, p.nc);
   } else {
     auto k = chunk_scan_simt_kernel<float, float>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     k<<<grid, 256, smem, st>>>(static_cast<const float*>(x), static_cast<const float*>(B),
                                static_cast<const float*>(C), D, cs2, dtT,
                                static_cast<const float*>(hprev), static_cast<float*>(y), p.L, p.H,
