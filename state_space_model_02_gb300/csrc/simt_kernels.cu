@@ -95,34 +95,34 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
     }
 }
 
-// grid: x = 64-row tile of the chunk, y = h, z = b * nc + c; dynamic shared memory holds the
-// masked matrix of the tile's rows, transposed: GsT[j][i] = 2^{cs2_i - cs2_j} dt_j (C_i . B_j)
-// for j <= i (0 above the diagonal), j < jmax.
+// grid: x = b * nc + c, y = 64-row tile of the chunk, z = group * head_split + part.  The
+// CTA computes the tile's causal C_i . B_j (j <= i, j < jmax) once -- it is the same for every
+// head of the group -- into dynamic shared memory, transposed (CBs[j][i]), then runs the heads
+// [part * per, (part + 1) * per) of the group.  Per head the decay 2^{cs2_i - cs2_j} dt_j is
+// applied in blocks of KT columns j starting at j0: 2^{cs2_j0 - cs2_j} dt_j (>= 0, at most
+// 2^{KT max|dt A| log2 e}) scales the staged x rows and 2^{cs2_i - cs2_j0} (<= 1 for
+// i >= j0, 0 for rows above the block) scales the block's partial sums, so no per-head
+// matrix is formed and no factor overflows.
 template <typename IO, typename HT>
 __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const IO* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ cs2, const float* __restrict__ dtT,
     const HT* __restrict__ hprev, IO* __restrict__ y, int64_t L, int64_t H, int64_t P, int64_t N,
-    int64_t G, int64_t Q, int64_t nc) {
-  extern __shared__ __align__(16) float GsT[];  // [jmax][GS]
+    int64_t G, int64_t Q, int64_t nc, int64_t head_split) {
+  extern __shared__ __align__(16) float CBs[];  // [jmax][GS]
   __shared__ __align__(16) float As[KT][TM];
   __shared__ __align__(16) float Bs[KT][TM];
   __shared__ float cs_i[TM], e_i[TM];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int64_t i0 = int64_t(blockIdx.x) * TM;
-  const int64_t h = blockIdx.y, bc = blockIdx.z, b = bc / nc, c = bc % nc;
-  const int64_t g = h / (H / G);
-  const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
-  const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
+  const int64_t i0 = int64_t(blockIdx.y) * TM;
+  const int64_t bc = blockIdx.x, b = bc / nc, c = bc % nc;
+  const int64_t g = blockIdx.z / head_split, part = blockIdx.z % head_split;
+  const int64_t hpg = H / G, per = (hpg + head_split - 1) / head_split;
+  const int64_t h_begin = g * hpg + part * per, h_end = min(g * hpg + hpg, h_begin + per);
   const int64_t jmax = i0 + TM < Q ? i0 + TM : Q;  // columns j < jmax can be causal for these rows
-  if (tid < TM) {
-    const bool in = i0 + tid < Q;
-    cs_i[tid] = in ? csr[i0 + tid] : 0.f;
-    e_i[tid] = in ? ex2(csr[i0 + tid]) : 0.f;
-  }
   auto row_ok = [&](int64_t i_chunk) { return i_chunk < Q && c * Q + i_chunk < L; };
 
-  // Phase 1: C_i . B_j over n, masked and decayed, into GsT
+  // Phase 1: the causal C . B^T of the tile's rows, head-independent
   for (int64_t j0 = 0; j0 < jmax; j0 += TM) {
     float acc[4][4] = {};
     for (int64_t n0 = 0; n0 < N; n0 += KT) {
@@ -143,62 +143,77 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
     for (int cc = 0; cc < 4; ++cc) {
       const int64_t j = j0 + 4 * tx + cc;
       if (j >= jmax) continue;
-      const float cj = j < Q ? csr[j] : 0.f, dj = j < Q ? dtr[j] : 0.f;
       float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] = (j <= i0 + 4 * ty + r) ? acc[r][cc] : 0.f;
+      *reinterpret_cast<float4*>(&CBs[j * GS + 4 * ty]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+
+  for (int64_t h = h_begin; h < h_end; ++h) {
+    const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
+    const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
+    __syncthreads();  // CBs complete / the previous head done with cs_i, As, Bs
+    if (tid < TM) {
+      const bool in = i0 + tid < Q;
+      cs_i[tid] = in ? csr[i0 + tid] : 0.f;
+      e_i[tid] = in ? ex2(csr[i0 + tid]) : 0.f;
+    }
+    __syncthreads();
+    const float Dh = D ? D[h] : 0.f;
+    const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
+    for (int64_t p0 = 0; p0 < P; p0 += TM) {
+      float acc1[4][4] = {}, acc2[4][4] = {};
+      for (int64_t j0 = 0; j0 < jmax; j0 += KT) {
+        const float cj0 = csr[j0];
+        for (int e = tid; e < KT * TM; e += 256) {
+          const int k = e / TM, col = e % TM;
+          const int64_t tj = j0 + k;
+          float v = 0.f;
+          if (row_ok(tj) && p0 + col < P)
+            v = ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) * (ex2(cj0 - csr[tj]) * dtr[tj]);
+          Bs[k][col] = v;
+        }
+        __syncthreads();
+        float part_acc[4][4] = {};
+#pragma unroll
+        for (int k = 0; k < KT; ++k)
+          mma4x4(part_acc, *reinterpret_cast<const float4*>(&CBs[(j0 + k) * GS + 4 * ty]),
+                 *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int il = 4 * ty + r;
+          const float rf = (j0 <= i0 + il) ? ex2(cs_i[il] - cj0) : 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(rf, part_acc[r][cc], acc1[r][cc]);
+        }
+        __syncthreads();
+      }
+      for (int64_t n0 = 0; n0 < N; n0 += KT) {
+        for (int e = tid; e < KT * TM; e += 256) {
+          const int r = e / KT, k = e % KT;
+          const int64_t n = n0 + k, ti = i0 + r;
+          As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
+          Bs[k][r] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < KT; ++k)
+          mma4x4(acc2, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+        __syncthreads();
+      }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int il = 4 * ty + r;
-        v[r] = (j <= i0 + il) ? acc[r][cc] * ex2(cs_i[il] - cj) * dj : 0.f;
-      }
-      *reinterpret_cast<float4*>(&GsT[j * GS + 4 * ty]) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  }
-  __syncthreads();
-
-  // Phase 2, per 64-column tile of p: y = GsT^T x + 2^{cs2_i} C hprev^T + D x
-  const float Dh = D ? D[h] : 0.f;
-  const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
-  for (int64_t p0 = 0; p0 < P; p0 += TM) {
-    float acc1[4][4] = {}, acc2[4][4] = {};
-    for (int64_t k0 = 0; k0 < jmax; k0 += KT) {
-      for (int e = tid; e < KT * TM; e += 256) {
-        const int k = e / TM, col = e % TM;
-        const int64_t tj = k0 + k;
-        Bs[k][col] = (tj < jmax && row_ok(tj) && p0 + col < P) ? ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) : 0.f;
-      }
-      __syncthreads();
+        const int64_t ti = i0 + il;
+        if (!row_ok(ti)) continue;
 #pragma unroll
-      for (int k = 0; k < KT; ++k) {
-        if (k0 + k < jmax)
-          mma4x4(acc1, *reinterpret_cast<const float4*>(&GsT[(k0 + k) * GS + 4 * ty]),
-                 *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
-      }
-      __syncthreads();
-    }
-    for (int64_t n0 = 0; n0 < N; n0 += KT) {
-      for (int e = tid; e < KT * TM; e += 256) {
-        const int r = e / KT, k = e % KT;
-        const int64_t n = n0 + k, ti = i0 + r;
-        As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
-        Bs[k][r] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < KT; ++k)
-        mma4x4(acc2, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
-      __syncthreads();
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int il = 4 * ty + r;
-      const int64_t ti = i0 + il;
-      if (!row_ok(ti)) continue;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int64_t p = p0 + 4 * tx + cc;
-        if (p < P) {
-          const int64_t off = ((b * L + c * Q + ti) * H + h) * P + p;
-          st_io(y, off, acc1[r][cc] + e_i[il] * acc2[r][cc] + Dh * ld_io(x, off));
+        for (int cc = 0; cc < 4; ++cc) {
+          const int64_t p = p0 + 4 * tx + cc;
+          if (p < P) {
+            const int64_t off = ((b * L + c * Q + ti) * H + h) * P + p;
+            st_io(y, off, acc1[r][cc] + e_i[il] * acc2[r][cc] + Dh * ld_io(x, off));
+          }
         }
       }
     }
@@ -227,8 +242,16 @@ cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void*
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>((p.Q + TM - 1) / TM), static_cast<unsigned>(p.H),
-                  static_cast<unsigned>(p.b * p.nc));
+  // split a group's heads over CTAs only as far as needed to give every SM two CTAs
+  const int64_t row_tiles = (p.Q + TM - 1) / TM, base = row_tiles * p.b * p.nc * p.G;
+  int sms = num_sms_current_device();
+  if (sms <= 0) sms = 1;
+  int64_t split = (2 * sms + base - 1) / base;
+  if (split > p.hpg) split = p.hpg;
+  if (split < 1) split = 1;
+  if (p.G * split > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(p.b * p.nc), static_cast<unsigned>(row_tiles),
+                  static_cast<unsigned>(p.G * split));
   const size_t smem = static_cast<size_t>(p.Q) * GS * sizeof(float);
   cudaError_t e;
   if (p.io_bf16) {
@@ -238,7 +261,7 @@ cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* 
     k<<<grid, 256, smem, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(B),
                                static_cast<const uint16_t*>(C), D, cs2, dtT,
                                static_cast<const uint16_t*>(hprev), static_cast<uint16_t*>(y), p.L,
-                               p.H, p.P, p.N, p.G, p.Q, p.nc);
+                               p.H, p.P, p.N, p.G, p.Q, p.nc, split);
   } else {
     auto k = chunk_scan_simt_kernel<float, float>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -246,7 +269,7 @@ cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* 
     k<<<grid, 256, smem, st>>>(static_cast<const float*>(x), static_cast<const float*>(B),
                                static_cast<const float*>(C), D, cs2, dtT,
                                static_cast<const float*>(hprev), static_cast<float*>(y), p.L, p.H,
-                               p.P, p.N, p.G, p.Q, p.nc);
+                               p.P, p.N, p.G, p.Q, p.nc, split);
   }
   return cudaGetLastError();
 }
