@@ -560,11 +560,19 @@ def run_ours(args):
         "roofline": roofline,
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in kern[n].items()}
                     for n in KERNELS},
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": len(KERNELS) * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": (len(KERNELS) - 1 + scan_launches(shape, plan)) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def scan_launches(shape, plan):
+    """Launches of the chunk_scan step: the tensor-core kernel runs once per 128 state columns
+    (plus one summing launch) when the state is larger than 128."""
+    n = shape["dstate"]
+    return n // 128 + 1 if (plan & 2) and n > 128 else 1
 
 
 def run_bwd(args, torch, dist, ssd, synth, ws, rank, local, dev):

@@ -33,7 +33,10 @@
 // barriers, so Y1's MMAs on group k overlap the mask writing group k+1.
 // Every wait is bounded; after an expiry all roles keep their loop trip counts (so named
 // barriers stay matched) but skip their work, then drain and release TMEM.
-// Requirements (chunk_scan_tc_ok): bf16 I/O, P = 64, Q in {128, 256}, N in {64, 128}.
+// Requirements (chunk_scan_tc_ok): bf16 I/O, P = 64, Q in {128, 256}, N in {64, 128}, or N a
+// multiple of 128 up to 512: y is linear in the state columns (CB and Y2 are sums over them, the
+// mask and the decays act element-wise), so larger states run one launch per 128-column slice,
+// D on the first only, into bf16 partial outputs that a last kernel sums in float32.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -50,6 +53,7 @@ constexpr uint32_t kBarMask = 1, kBarEpi = 2;  // named barriers of the mask and
 
 struct ScParams {
   int32_t L, H, nc, Q, N, hpg, MT;
+  int32_t col0;  // first state column of this launch's slice (C and B are N columns per group)
   int64_t units, total_weight;
   const float* cs2;
   const float* dtT;
@@ -187,12 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i0 = sg.mt * 128, jrows = i0 + 128;
         mbar_arrive_expect_tx(bar(kCbFull), NB * kBox128 + NB * jrows * 128);
         for (int nb = 0; nb < NB; ++nb)
-          tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + nb * 64,
+          tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + prm.col0 + nb * 64,
                       sg.c * Q + i0, sg.b);
         for (int nb = 0; nb < NB; ++nb)
           for (int jb = 0; jb < jrows / 128; ++jb)
             tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar(kCbFull),
-                        sg.g * N + nb * 64, sg.c * Q + jb * 128, sg.b);
+                        sg.g * N + prm.col0 + nb * 64, sg.c * Q + jb * 128, sg.b);
       };
       // x slot s of a head: its x box(es) now, its cs2 / dt rows (from the previous kernel) later;
       // the slot's barrier expects all three from the start
@@ -497,18 +501,67 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
                     maps[4], prm);
 }
 
+// y = the sum of the slices' bf16 partial outputs, accumulated in float32 and rounded once
+__global__ void sum_slices_kernel(const uint4* __restrict__ parts, uint4* __restrict__ y, int64_t n8,
+                                  int64_t slices) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  float acc[8] = {};
+  for (int64_t s = 0; s < slices; ++s) {
+    const uint4 v = __ldg(parts + s * n8 + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[2 * k] += bf16lo_to_f32(w[k]);
+      acc[2 * k + 1] += bf16hi_to_f32(w[k]);
+    }
+  }
+  y[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                    pack_bf16x2(acc[6], acc[7]));
+}
+
 }  // namespace
 
 bool chunk_scan_tc_ok(const Problem& p) {
-  return p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) && (p.N == 64 || p.N == 128) &&
-         p.L <= (int64_t(1) << 31) - 1 && p.b * p.nc * p.H * p.P < (int64_t(1) << 31) &&
-         p.G * p.N < (int64_t(1) << 31);
+  return p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) &&
+         (p.N == 64 || p.N == 128 || scan_slices(p) > 1) && p.L <= (int64_t(1) << 31) - 1 &&
+         p.b * p.nc * p.H * p.P < (int64_t(1) << 31) && p.G * p.N < (int64_t(1) << 31);
 }
+
+cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
+                                       const float* D, const float* cs2, const float* dtT,
+                                       const void* hprev, void* y, uint32_t* status, cudaStream_t st,
+                                       const char** why, int32_t col0, int32_t width);
 
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
                                  const float* D, const float* cs2, const float* dtT,
-                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
-                                 const char** why) {
+                                 const void* hprev, void* y, void* yparts, uint32_t* status,
+                                 cudaStream_t st, const char** why) {
+  const int64_t slices = scan_slices(p);
+  if (slices > 1) {
+    // one launch per 128-column slice of the state, into bf16 partial outputs, then their sum
+    const int64_t n_y = p.b * p.L * p.H * p.P;
+    for (int64_t s = 0; s < slices; ++s) {
+      const cudaError_t e = launch_chunk_scan_tc_slice(
+          p, x, B, C, s == 0 ? D : nullptr, cs2, dtT, static_cast<const uint16_t*>(hprev) + 128 * s,
+          static_cast<uint16_t*>(yparts) + s * n_y, status, st, why, static_cast<int32_t>(128 * s), 128);
+      if (e != cudaSuccess) return e;
+    }
+    const int64_t n8 = n_y / 8;
+    sum_slices_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint4*>(yparts), static_cast<uint4*>(y), n8, slices);
+    return cudaGetLastError();
+  }
+  return launch_chunk_scan_tc_slice(p, x, B, C, D, cs2, dtT, hprev, y, status, st, why, 0,
+                                    static_cast<int32_t>(p.N));
+}
+
+// One launch over the state columns col0 .. col0 + width - 1 (width 64 or 128); hprev points at
+// column col0 of the full state rows.
+cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
+                                       const float* D, const float* cs2, const float* dtT,
+                                       const void* hprev, void* y, uint32_t* status, cudaStream_t st,
+                                       const char** why, int32_t col0, int32_t width) {
   CUtensorMap maps[5];  // x, B, C, hprev, y
   const uint64_t xdims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t xstr[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
@@ -517,9 +570,9 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   const uint32_t box3[3] = {64, 128, 1};
   // hprev (rows p of each (b, c, h), N columns) as (64 columns, rows, N / 64 column halves), so
   // that one box {64, 64, N / 64} lands as N / 64 swizzled 8 KB tiles
-  const uint64_t hdims[3] = {64, uint64_t(p.b * p.nc * p.H * p.P), uint64_t(p.N / 64)};
+  const uint64_t hdims[3] = {64, uint64_t(p.b * p.nc * p.H * p.P), uint64_t(width / 64)};
   const uint64_t hstr[2] = {uint64_t(p.N * 2), 128};
-  const uint32_t hbox[3] = {64, 64, uint32_t(p.N / 64)};
+  const uint32_t hbox[3] = {64, 64, uint32_t(width / 64)};
   if (!encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, bdims, bstr, box3,
@@ -537,6 +590,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   prm.nc = static_cast<int32_t>(p.nc);
   prm.Q = static_cast<int32_t>(p.Q);
   prm.N = static_cast<int32_t>(p.N);
+  prm.col0 = col0;
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.MT = static_cast<int32_t>(p.Q / 128);
   prm.units = p.b * p.nc * prm.MT * p.H;
@@ -549,7 +603,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
   int sms = num_sms_current_device();
   if (sms <= 0) sms = 1;
   const int grid = static_cast<int>(prm.units < sms ? prm.units : sms);
-  if (p.N == 64) return launch_nb<1>(maps, prm, grid, st);
+  if (width == 64) return launch_nb<1>(maps, prm, grid, st);
   return launch_nb<2>(maps, prm, grid, st);
 }
 

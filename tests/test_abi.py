@@ -103,8 +103,11 @@ def test_status_strings(lib):
 def test_kernel_plan(lib):
     assert ssd.kernel_plan(shape()) == 3                              # both steps on tensor cores
     assert ssd.kernel_plan(shape(batch=4, seqlen=2048, nheads=24)) == 3
-    assert ssd.kernel_plan(shape(dstate=256)) in (1, 3)
-    assert ssd.kernel_plan(shape(dstate=512)) in (1, 3)
+    assert ssd.kernel_plan(shape(dstate=256)) & 2                     # sliced tensor-core chunk_scan
+    assert ssd.kernel_plan(shape(dstate=384)) & 2
+    assert ssd.kernel_plan(shape(dstate=512)) & 2
+    assert not ssd.kernel_plan(shape(dstate=640)) & 2                 # above 512: CUDA-core chunk_scan
+    assert not ssd.kernel_plan(shape(dstate=192)) & 2                 # not a multiple of 128
     assert ssd.kernel_plan(shape(flags=ssd.FLAG_FORCE_SIMT)) == 0
     assert ssd.kernel_plan(shape(io_dtype=ssd.SSD_F32)) == 0          # exact-fp32 CUDA-core path
     assert ssd.kernel_plan(shape(headdim=32)) == 0

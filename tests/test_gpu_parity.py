@@ -108,6 +108,8 @@ EDGE = [
     dict(batch=1, seqlen=512, nheads=6, headdim=64, dstate=128, ngroups=2, chunk=256),  # 3 heads per group
     dict(batch=1, seqlen=300, nheads=3, headdim=32, dstate=48, chunk=64),      # CUDA-core path shapes
     dict(batch=1, seqlen=700, nheads=2, headdim=64, dstate=256, chunk=256),
+    dict(batch=2, seqlen=600, nheads=3, headdim=64, dstate=384, chunk=128),   # three state slices
+    dict(batch=1, seqlen=520, nheads=4, headdim=64, dstate=256, ngroups=2, chunk=256),  # slices x groups
 ]
 
 
@@ -134,6 +136,16 @@ def test_no_D_and_no_init():
 def test_tensor_core_and_cuda_core_paths_agree():
     inp = synth.make_inputs(batch=2, seqlen=1024, nheads=4, headdim=64, dstate=128, chunk=256,
                             io_dtype="bf16", init=True, seed=11)
+    y_tc, f_tc = run(inp)
+    y_sc, f_sc = run(inp, flags=ssd.FLAG_FORCE_SIMT)
+    assert rel(y_tc, y_sc) <= 2e-2 and rel(f_tc, f_sc) <= 2e-2
+
+
+@pytest.mark.parametrize("n", [256, 512])
+def test_sliced_tensor_core_scan_matches_cuda_core(n):
+    # state sizes above 128 run the tensor-core chunk_scan once per 128-column slice
+    inp = synth.make_inputs(batch=1, seqlen=1000, nheads=4, headdim=64, dstate=n, chunk=256,
+                            io_dtype="bf16", init=True, seed=13)
     y_tc, f_tc = run(inp)
     y_sc, f_sc = run(inp, flags=ssd.FLAG_FORCE_SIMT)
     assert rel(y_tc, y_sc) <= 2e-2 and rel(f_tc, f_sc) <= 2e-2
