@@ -570,9 +570,9 @@ def run_ours(args):
 
 def scan_launches(shape, plan):
     """Launches of the chunk_scan step: the tensor-core kernel runs once per 128 state columns
-    (plus one summing launch) when the state is larger than 128."""
+    when the state is larger than 128."""
     n = shape["dstate"]
-    return n // 128 + 1 if (plan & 2) and n > 128 else 1
+    return n // 128 if (plan & 2) and n > 128 else 1
 
 
 def run_bwd(args, torch, dist, ssd, synth, ws, rank, local, dev):

@@ -36,7 +36,7 @@
 // Requirements (chunk_scan_tc_ok): bf16 I/O, P = 64, Q in {128, 256}, N in {64, 128}, or N a
 // multiple of 128 up to 512: y is linear in the state columns (CB and Y2 are sums over them, the
 // mask and the decays act element-wise), so larger states run one launch per 128-column slice,
-// D on the first only, into bf16 partial outputs that a last kernel sums in float32.
+// D on the first only; each later slice's epilogue adds the bf16 y its predecessors stored.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -55,6 +55,7 @@ struct ScParams {
   int32_t L, H, nc, Q, N, hpg, MT;
   int32_t col0;  // first state column of this launch's slice (C and B are N columns per group)
   int64_t units, total_weight;
+  const uint16_t* yacc;  // y of the previous slices, added to this one's (null: first slice)
   const float* cs2;
   const float* dtT;
   const float* D;
@@ -438,6 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = gi & 1;
         // this row's cs2 (one coalesced L2 read per warp), fetched while the MMAs finish
         const float cs_i = __ldg(prm.cs2 + ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q + row);
+        // and, for a later state slice, the row of y the earlier slices wrote (a plain load: the
+        // buffer is this kernel's output too)
+        uint4 prev[8];
+        if (prm.yacc && int64_t(sg.c) * Q + row < prm.L) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              prm.yacc + ((int64_t(sg.b) * prm.L + int64_t(sg.c) * Q + row) * H + hh) * 64);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) prev[k] = src[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) prev[k] = make_uint4(0, 0, 0, 0);
+        }
         const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && !*abort_flag;
         tc_fence_after();
         if (store_thread) bulk_wait_read0();  // the staging buffer is free again
@@ -455,12 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               const int cc = 2 * quarter + c2;
+              const uint32_t pw[4] = {prev[cc].x, prev[cc].y, prev[cc].z, prev[cc].w};
               uint32_t o[4];
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
                 const int k0 = 8 * c2 + 2 * e2;
-                o[e2] = pack_bf16x2(__uint_as_float(a[k0]) + e * __uint_as_float(q2[k0]),
-                                    __uint_as_float(a[k0 + 1]) + e * __uint_as_float(q2[k0 + 1]));
+                o[e2] = pack_bf16x2(__uint_as_float(a[k0]) + e * __uint_as_float(q2[k0]) + bf16lo_to_f32(pw[e2]),
+                                    __uint_as_float(a[k0 + 1]) + e * __uint_as_float(q2[k0 + 1]) +
+                                        bf16hi_to_f32(pw[e2]));
               }
               *reinterpret_cast<uint4*>(ys + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -501,25 +516,6 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
                     maps[4], prm);
 }
 
-// y = the sum of the slices' bf16 partial outputs, accumulated in float32 and rounded once
-__global__ void sum_slices_kernel(const uint4* __restrict__ parts, uint4* __restrict__ y, int64_t n8,
-                                  int64_t slices) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  float acc[8] = {};
-  for (int64_t s = 0; s < slices; ++s) {
-    const uint4 v = __ldg(parts + s * n8 + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[2 * k] += bf16lo_to_f32(w[k]);
-      acc[2 * k + 1] += bf16hi_to_f32(w[k]);
-    }
-  }
-  y[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                    pack_bf16x2(acc[6], acc[7]));
-}
-
 }  // namespace
 
 bool chunk_scan_tc_ok(const Problem& p) {
@@ -530,38 +526,32 @@ bool chunk_scan_tc_ok(const Problem& p) {
 
 cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
                                        const float* D, const float* cs2, const float* dtT,
-                                       const void* hprev, void* y, uint32_t* status, cudaStream_t st,
-                                       const char** why, int32_t col0, int32_t width);
+                                       const void* hprev, void* y, const void* yacc, uint32_t* status,
+                                       cudaStream_t st, const char** why, int32_t col0, int32_t width);
 
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
                                  const float* D, const float* cs2, const float* dtT,
-                                 const void* hprev, void* y, void* yparts, uint32_t* status,
-                                 cudaStream_t st, const char** why) {
+                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
+                                 const char** why) {
   const int64_t slices = scan_slices(p);
-  if (slices > 1) {
-    // one launch per 128-column slice of the state, into bf16 partial outputs, then their sum
-    const int64_t n_y = p.b * p.L * p.H * p.P;
-    for (int64_t s = 0; s < slices; ++s) {
-      const cudaError_t e = launch_chunk_scan_tc_slice(
-          p, x, B, C, s == 0 ? D : nullptr, cs2, dtT, static_cast<const uint16_t*>(hprev) + 128 * s,
-          static_cast<uint16_t*>(yparts) + s * n_y, status, st, why, static_cast<int32_t>(128 * s), 128);
-      if (e != cudaSuccess) return e;
-    }
-    const int64_t n8 = n_y / 8;
-    sum_slices_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
-        static_cast<const uint4*>(yparts), static_cast<uint4*>(y), n8, slices);
-    return cudaGetLastError();
+  // one launch per 128-column slice of the state; each later slice adds the y its predecessors
+  // left (the launches are stream-ordered, and each waits for the previous grid before reading)
+  for (int64_t s = 0; s < slices; ++s) {
+    const int32_t width = slices > 1 ? 128 : static_cast<int32_t>(p.N);
+    const cudaError_t e = launch_chunk_scan_tc_slice(
+        p, x, B, C, s == 0 ? D : nullptr, cs2, dtT, static_cast<const uint16_t*>(hprev) + width * s, y,
+        s == 0 ? nullptr : y, status, st, why, static_cast<int32_t>(width * s), width);
+    if (e != cudaSuccess) return e;
   }
-  return launch_chunk_scan_tc_slice(p, x, B, C, D, cs2, dtT, hprev, y, status, st, why, 0,
-                                    static_cast<int32_t>(p.N));
+  return cudaSuccess;
 }
 
 // One launch over the state columns col0 .. col0 + width - 1 (width 64 or 128); hprev points at
 // column col0 of the full state rows.
 cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
                                        const float* D, const float* cs2, const float* dtT,
-                                       const void* hprev, void* y, uint32_t* status, cudaStream_t st,
-                                       const char** why, int32_t col0, int32_t width) {
+                                       const void* hprev, void* y, const void* yacc, uint32_t* status,
+                                       cudaStream_t st, const char** why, int32_t col0, int32_t width) {
   CUtensorMap maps[5];  // x, B, C, hprev, y
   const uint64_t xdims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t xstr[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
@@ -591,6 +581,7 @@ cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const vo
   prm.Q = static_cast<int32_t>(p.Q);
   prm.N = static_cast<int32_t>(p.N);
   prm.col0 = col0;
+  prm.yacc = static_cast<const uint16_t*>(yacc);
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.MT = static_cast<int32_t>(p.Q / 128);
   prm.units = p.b * p.nc * prm.MT * p.H;

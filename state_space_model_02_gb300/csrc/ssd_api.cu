@@ -63,7 +63,6 @@ struct Views {
   float* dtT;
   void* S;  // per-chunk states, in the I/O dtype
   void* hprev;
-  void* yparts;  // per-slice outputs of the sliced tensor-core chunk_scan (state sizes > 128)
 };
 
 ssd_status carve(const ssd::Problem& p, void* ws, size_t ws_bytes, Views* v) {
@@ -78,7 +77,6 @@ ssd_status carve(const ssd::Problem& p, void* ws, size_t ws_bytes, Views* v) {
   v->dtT = reinterpret_cast<float*>(base + l.dtT);
   v->S = base + l.S;
   v->hprev = base + l.hprev;
-  v->yparts = base + l.yparts;
   return SSD_OK;
 }
 
@@ -121,7 +119,7 @@ ssd_status step_scan(const ssd::Problem& p, const void* x, const void* B, const 
   cudaError_t e;
   if (use_scan_tc(p)) {
     const char* why = nullptr;
-    e = ssd::launch_chunk_scan_tc(p, x, B, C, D, v.cs2, v.dtT, v.hprev, y, v.yparts, v.status, st, &why);
+    e = ssd::launch_chunk_scan_tc(p, x, B, C, D, v.cs2, v.dtT, v.hprev, y, v.status, st, &why);
     if (why) return fail(SSD_ERR_CUDA, "chunk_scan: %s", why);
   } else {
     e = ssd::launch_chunk_scan_simt(p, x, B, C, D, v.cs2, v.dtT, v.hprev, y, st);

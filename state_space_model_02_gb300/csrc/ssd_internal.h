@@ -25,7 +25,7 @@ struct SelProblem {
 
 // Byte offsets inside the caller's workspace.  Each region is 1024-byte aligned.
 struct Layout {
-  size_t status, cs2, dtT, S, hprev, yparts, total;
+  size_t status, cs2, dtT, S, hprev, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -33,7 +33,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // The tensor-core chunk_scan keeps C and hprev resident for 64 or 128 state columns.  Larger
 // state sizes (a multiple of 128, up to 512) run it once per 128-column slice -- the products
 // C.B^T and C.hprev^T are sums over the state dimension and the mask and decays act element-wise
-// -- into bf16 partial outputs summed by one more kernel.
+// -- each later slice adding the y of the earlier ones.
 inline int64_t scan_slices(const Problem& p) {
   return (p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) && p.N > 128 && p.N % 128 == 0 &&
           p.N <= 512)
@@ -45,15 +45,12 @@ inline Layout make_layout(const Problem& p) {
   Layout l{};
   const size_t cs_bytes = static_cast<size_t>(p.b * p.H * p.nc * p.Q) * 4u;
   const size_t st_elems = static_cast<size_t>(p.b * p.nc * p.H * p.P * p.N);
-  const int64_t slices = scan_slices(p);
   l.status = 0;
   l.cs2 = 1024;
   l.dtT = align_up(l.cs2 + cs_bytes, 1024);
   l.S = align_up(l.dtT + cs_bytes, 1024);
   l.hprev = align_up(l.S + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
-  l.yparts = align_up(l.hprev + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
-  const size_t yparts_bytes = slices > 1 ? static_cast<size_t>(slices * p.b * p.L * p.H * p.P) * 2u : 0u;
-  l.total = align_up(l.yparts + yparts_bytes, 1024);
+  l.total = align_up(l.hprev + st_elems * (p.io_bf16 ? 2u : 4u), 1024);
   return l;
 }
 
@@ -138,7 +135,7 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
 
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
                                  const float* D, const float* cs2, const float* dtT,
-                                 const void* hprev, void* y, void* yparts, uint32_t* status, cudaStream_t st,
+                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
                                  const char** why);
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
