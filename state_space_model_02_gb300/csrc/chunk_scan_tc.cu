@@ -24,11 +24,13 @@
 //               is done; one box) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are
 //               done).  A TMA box costs the SM about the same for 64 or 128 rows, so operands
 //               come in few, large boxes and nothing is prefetched separately;
-//   warp 1      tcgen05.mma issuer; owns the TMEM allocation
-//   warps 2-9   mask: CB (TMEM) -> P (bf16, shared memory) for head h+1 ...
-//   warps 10-13 epilogue: ... while these finish head h: y = Y1 + 2^{cs2_i} Y2 -> TMA store
-// A warp reads the TMEM lane quarter (warp % 4): two mask warps share each quarter and take
-// alternate 32-column blocks; the four epilogue warps cover the 128 rows once.  P is handed to
+//   warp 1      tcgen05.mma issuer; owns the TMEM allocation.  It touches no shared memory
+//               between MMAs (such an access waits for the MMAs already queued): warp 22
+//               waits on its mbarriers and hands over through a named barrier
+//   warps 2-17  mask: CB (TMEM) -> P (bf16, shared memory) for head h+1 ...
+//   warps 18-21 epilogue: ... while these finish head h: y = Y1 + 2^{cs2_i} Y2 -> TMA store
+// A warp reads the TMEM lane quarter (warp % 4): four mask warps share each quarter and take
+// its 32-column blocks round-robin; the four epilogue warps cover the 128 rows once.  P is handed to
 // the MMA issuer in four 64-column groups (one 16 KB swizzle atom each) with their own
 // barriers, so Y1's MMAs on group k overlap the mask writing group k+1.
 // Every wait is bounded; after an expiry all roles keep their loop trip counts (so named
@@ -43,13 +45,32 @@
 namespace ssd {
 namespace {
 
-constexpr int kMaskWarps = 8, kEpiWarps = 4;  // warps 2-9 mask, 10-13 epilogue
-constexpr int kWarps = 2 + kMaskWarps + kEpiWarps;
+constexpr int kMaskWarps = 16, kEpiWarps = 4;  // warps 2-17 mask, 18-21 epilogue, 22 poller
+constexpr int kPollWarp = 2 + kMaskWarps + kEpiWarps;
+constexpr int kWarps = kPollWarp + 1;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kBox128 = 16384;  // TMA box: 128 rows x 128 bytes
 constexpr uint32_t kBox64 = 8192;    // TMA box: 64 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;  // CB [0,256) | Y1 buf0 | Y2 buf0 | Y1 buf1 | Y2 buf1
-constexpr uint32_t kBarMask = 1, kBarEpi = 2;  // named barriers of the mask and epilogue groups
+// named barriers: the mask group, the epilogue group, and the poller -> MMA issuer handoff
+constexpr uint32_t kBarMask = 1, kBarEpi = 2, kBarIssue = 3;
+
+// One handoff from the poller warp to the MMA-issuing warp: both warps (64 threads) arrive and
+// both get the AND of their flags (the poller's "the awaited barriers completed and the CTA has
+// not aborted"; the issuer passes true).  The barrier also orders the poller's acquire of those
+// mbarriers before the issuer's following tcgen05 operations (with tcgen05.fence::after_thread_sync).
+__device__ __forceinline__ bool issue_handoff(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u), "n"(kBarIssue), "n"(64)
+      : "memory");
+  return r != 0u;
+}
 
 struct ScParams {
   int32_t L, H, nc, Q, N, hpg, MT;
@@ -127,6 +148,33 @@ __device__ __forceinline__ Segment segment_at(int64_t u, int64_t u_end, const Sc
   const int64_t h_end = min(int64_t((s.g + 1) * prm.hpg), s.h_begin + (u_end - u));
   s.nh = static_cast<int>(h_end - s.h_begin);
   return s;
+}
+
+// One 32 x 32 block of P for this thread's row: P[row, j0 + e] = CB[row, j0 + e] * colf[e] *
+// rowf, rounded to bf16 and stored as four 16-byte chunks of the row's 128-byte swizzled line.
+// DIAG: the block holding the diagonal (column dr = row - j0): zero right of it, + D_h on it.
+template <bool DIAG>
+__device__ __forceinline__ void mask_block(const uint32_t (&v)[32], const float* cf, float rowf, int dr,
+                                           float Dh, uint8_t* pb, int cbase, int r) {
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const float4 fa = reinterpret_cast<const float4*>(cf)[2 * c4];
+    const float4 fb = reinterpret_cast<const float4*>(cf)[2 * c4 + 1];
+    const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int e = 8 * c4 + 2 * e2;
+      float w0 = __uint_as_float(v[e]) * f[2 * e2] * rowf;
+      float w1 = __uint_as_float(v[e + 1]) * f[2 * e2 + 1] * rowf;
+      if (DIAG) {
+        w0 = e > dr ? 0.f : (e == dr ? w0 + Dh : w0);
+        w1 = e + 1 > dr ? 0.f : (e + 1 == dr ? w1 + Dh : w1);
+      }
+      o[e2] = pack_bf16x2(w0, w1);
+    }
+    *reinterpret_cast<uint4*>(pb + (((cbase + c4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 template <int NB>
@@ -269,14 +317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t gi = 0, si = 0, gpar = 0;  // gpar bit k: parity of P group k's uses so far
-      for (int64_t u = u_begin; u < u_end; ++si) {
-        const Segment sg = segment_at(u, u_end, prm);
-        const int jrows = sg.mt * 128 + 128;
-        const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
-        const bool e = si == 0 || mbar_wait(bar(kCbEmpty), (si - 1) & 1, ctl);
-        if (a && e && !*abort_flag) {
+    // The whole warp walks the schedule and lane 0 issues.  It never waits on an mbarrier or
+    // reads the abort flag itself: a shared-memory access by the issuing thread stalls until its
+    // queued MMAs have completed, which would serialise the groups.  The poller warp waits and
+    // hands each "go" over through kBarIssue, at exactly the same points of the same schedule.
+    uint32_t gi = 0;
+    for (int64_t u = u_begin; u < u_end;) {
+      const Segment sg = segment_at(u, u_end, prm);
+      const int jrows = sg.mt * 128 + 128;
+      const bool go_cb = issue_handoff(true);
+      if (lane == 0) {
+        if (go_cb) {
           tc_fence_after();
           const uint32_t idesc = idesc_bf16_f32(128, jrows, 0, 0);
           for (int nb = 0; nb < NB; ++nb)
@@ -287,14 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (nb | k) != 0 ? 1u : 0u);
         }
         umma_commit(bar(kCbDone));
-        for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
-          const uint32_t s = gi & 1, use = gi >> 1;
-          const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
-          const uint32_t hp = sb + SM::kHp0 + s * SM::kHpBytes;
-          const uint32_t ycol = 256 + 128 * s;
-          const bool h = mbar_wait(bar(kHpFull0 + s), use & 1, ctl);
-          const bool y = gi < 2 || mbar_wait(bar(kYEmpty0 + s), (use - 1) & 1, ctl);
-          if (h && y && !*abort_flag) {
+      }
+      __syncwarp();
+      for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+        const uint32_t s = gi & 1;
+        const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
+        const uint32_t hp = sb + SM::kHp0 + s * SM::kHpBytes;
+        const uint32_t ycol = 256 + 128 * s;
+        const bool go_y2 = issue_handoff(true);
+        if (lane == 0) {
+          if (go_y2) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
             for (int nb = 0; nb < NB; ++nb)
@@ -304,11 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          sdesc_sw128(hp + nb * kBox64 + k * 32, 16, 1024), idesc, (nb | k) != 0 ? 1u : 0u);
           }
           umma_commit(bar(kHpEmpty0 + s));
-          const bool f = mbar_wait(bar(kXsFull0 + s), use & 1, ctl);
-          const uint32_t idesc1 = idesc_bf16_f32(128, 64, 0, 1);
-          for (int k = 0; k < jrows / 64; ++k) {
-            const bool p = mbar_wait(bar(kPFull0 + k), (gpar >> k) & 1u, ctl);
-            if (f && y && p && !*abort_flag) {
+        }
+        __syncwarp();
+        const uint32_t idesc1 = idesc_bf16_f32(128, 64, 0, 1);
+        for (int k = 0; k < jrows / 64; ++k) {
+          const bool go = issue_handoff(true);
+          if (lane == 0) {
+            if (go) {
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
@@ -317,22 +372,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                          (k | kk) != 0 ? 1u : 0u);
             }
             umma_commit(bar(kPEmpty0 + k));
-            gpar ^= 1u << k;
           }
+          __syncwarp();
+        }
+        if (lane == 0) {
           umma_commit(bar(kYFull0 + s));
           umma_commit(bar(kXsEmpty0 + s));
         }
-        umma_commit(bar(kSegFree));
-        u += sg.nh;
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(bar(kSegFree));
+      __syncwarp();
+      u += sg.nh;
+    }
+    if (lane == 0) {
       umma_commit(bar(kDrain));
       (void)mbar_drain(bar(kDrain), 0, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == kPollWarp) {
+    // ----------------------------------------------------- poller for the MMA issuer
+    // the issuer's waits, in its order; every wait is bounded, so every handoff is reached
+    uint32_t gi = 0, si = 0, gpar = 0;  // gpar bit k: parity of P group k's uses so far
+    for (int64_t u = u_begin; u < u_end; ++si) {
+      const Segment sg = segment_at(u, u_end, prm);
+      const int jrows = sg.mt * 128 + 128;
+      const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
+      const bool e = si == 0 || mbar_wait(bar(kCbEmpty), (si - 1) & 1, ctl);
+      (void)issue_handoff(a && e && !*abort_flag);
+      for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
+        const uint32_t s = gi & 1, use = gi >> 1;
+        const bool h = mbar_wait(bar(kHpFull0 + s), use & 1, ctl);
+        const bool y = gi < 2 || mbar_wait(bar(kYEmpty0 + s), (use - 1) & 1, ctl);
+        (void)issue_handoff(h && y && !*abort_flag);
+        const bool f = mbar_wait(bar(kXsFull0 + s), use & 1, ctl);
+        for (int k = 0; k < jrows / 64; ++k) {
+          const bool p = mbar_wait(bar(kPFull0 + k), (gpar >> k) & 1u, ctl);
+          (void)issue_handoff(f && y && p && !*abort_flag);
+          gpar ^= 1u << k;
+        }
+      }
+      u += sg.nh;
     }
   } else if (warp < 2 + kMaskWarps) {
     // ------------------------------------------------------------- mask: CB -> P in smem
     const int q = warp & 3, r = 32 * q + lane;  // TMEM lane quarter and m-tile row
-    const int sub = (warp - 2) >> 2;            // which of the quarter's two mask warps
-    const int mt_thread = (warp - 2) * 32 + lane;  // 0..255 over the mask group
+    const int sub = (warp - 2) >> 2;            // which of the quarter's four mask warps
+    const int mt_thread = (warp - 2) * 32 + lane;  // 0..511 over the mask group
     const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
     uint32_t gi = 0, si = 0;
     uint32_t gpar = 0, gused = 0;  // per P group: parity of its uses so far, used at least once
@@ -343,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (void)mbar_wait(bar(kCbDone), si & 1, ctl);
       tc_fence_after();
       // blocks right of this quarter's diagonal block stay zero for the whole segment
-      for (int blk = maxblk + 1 + sub; blk < nblk; blk += 2) {
+      for (int blk = maxblk + 1 + sub; blk < nblk; blk += 4) {
         const int j0 = 32 * blk;
         uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + r * 128;
 #pragma unroll
@@ -364,47 +450,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarMask, 32 * kMaskWarps);
         const bool live = have && !*abort_flag;
         tc_fence_after();
-        // group k holds 32-column blocks 2k and 2k+1; this warp owns block 2k + sub.  The TMEM
-        // load of the block is issued before the wait for the group's P buffer.
+        // group k holds 32-column blocks 2k and 2k+1; a quarter's four warps take its blocks
+        // round-robin (warp sub owns block 2k + (sub & 1) of the groups k with k % 2 == sub / 2),
+        // so two groups are written at once.  The TMEM load of the block is issued before the
+        // wait for the group's P buffer; a warp owning nothing in a group arrives at once (the
+        // head-start barrier keeps every warp within one head of the others).
         const int ng = jrows / 64;
 #pragma unroll 1
         for (int k = 0; k < ng; ++k) {
-          const int blk = 2 * k + sub, j0 = 32 * blk;
-          const bool mine = live && blk <= maxblk;
+          const bool owner = (k & 1) == (sub >> 1);
+          const int blk = 2 * k + (sub & 1), j0 = 32 * blk;
+          const bool mine = live && owner && blk <= maxblk;
           uint32_t v[32];
           if (mine) {
             __syncwarp();
             tmem_ld32(trow + j0, v);
           }
-          const bool pfree = !((gused >> k) & 1u) || mbar_wait(bar(kPEmpty0 + k), ((gpar >> k) & 1u) ^ 1u, ctl);
+          const bool pfree = !owner || !((gused >> k) & 1u) ||
+                             mbar_wait(bar(kPEmpty0 + k), ((gpar >> k) & 1u) ^ 1u, ctl);
           if (mine) tmem_ld_wait();
           if (mine && pfree) {
             // P[row, j] = CB[row, j] colf[j] 2^(cs2_row - cs2_j0), zero right of the diagonal,
             // plus D_h on it
             const float rowf = ex2(cs_i - cs[j0]);
-            const float2 rf = make_float2(rowf, rowf);
-            const bool diag = blk == maxblk;
-            const float4* cf = reinterpret_cast<const float4*>(colf + j0);
+            const float* cf = colf + j0;
             uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + r * 128;
             const int cbase = (j0 & 63) >> 3;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              const float4 fa = cf[2 * c4], fb = cf[2 * c4 + 1];
-              const float2 f2[4] = {make_float2(fa.x, fa.y), make_float2(fa.z, fa.w), make_float2(fb.x, fb.y),
-                                    make_float2(fb.z, fb.w)};
-              uint32_t o[4];
-#pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const int e = 8 * c4 + 2 * e2;
-                float2 w = mul_f32x2(mul_f32x2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2[e2]), rf);
-                if (diag) {
-                  w.x = j0 + e > row ? 0.f : (j0 + e == row ? w.x + Dh : w.x);
-                  w.y = j0 + e + 1 > row ? 0.f : (j0 + e + 1 == row ? w.y + Dh : w.y);
-                }
-                o[e2] = pack_bf16x2(w.x, w.y);
-              }
-              *reinterpret_cast<uint4*>(pb + (((cbase + c4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+            // one branch per block: the diagonal block masks j > row and adds D_h on j == row
+            if (blk == maxblk)
+              mask_block<true>(v, cf, rowf, row - j0, Dh, pb, cbase, r);
+            else
+              mask_block<false>(v, cf, rowf, 0, 0.f, pb, cbase, r);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -422,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kCbEmpty));
       u += sg.nh;
     }
-  } else {
+  } else if (warp < kPollWarp) {
     // ------------------------ epilogue: y = Y1 + 2^cs2_i Y2 -> staging -> TMA store of y
     // (D x already sits in Y1 through P's diagonal)
     const int q = warp & 3, r = 32 * q + lane;
@@ -441,16 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cs_i = __ldg(prm.cs2 + ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q + row);
         // and, for a later state slice, the row of y the earlier slices wrote (a plain load: the
         // buffer is this kernel's output too)
-        uint4 prev[8];
-        if (prm.yacc && int64_t(sg.c) * Q + row < prm.L) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              prm.yacc + ((int64_t(sg.b) * prm.L + int64_t(sg.c) * Q + row) * H + hh) * 64);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) prev[k] = src[k];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) prev[k] = make_uint4(0, 0, 0, 0);
-        }
+        const uint4* prev_row =
+            prm.yacc && int64_t(sg.c) * Q + row < prm.L
+                ? reinterpret_cast<const uint4*>(prm.yacc + ((int64_t(sg.b) * prm.L + int64_t(sg.c) * Q + row) * H + hh) * 64)
+                : nullptr;
         const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && !*abort_flag;
         tc_fence_after();
         if (store_thread) bulk_wait_read0();  // the staging buffer is free again
@@ -468,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               const int cc = 2 * quarter + c2;
-              const uint32_t pw[4] = {prev[cc].x, prev[cc].y, prev[cc].z, prev[cc].w};
+              const uint4 pv = prev_row ? prev_row[cc] : make_uint4(0, 0, 0, 0);
+              const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
               uint32_t o[4];
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
