@@ -20,10 +20,13 @@ namespace ssd {
 namespace {
 
 constexpr int kDepth = 8;
-// bf16x8 kernel: 64-thread CTAs and at most 56 registers (18 CTAs per SM), so that a layer's
-// columns fit in one wave of evenly loaded SMs (each thread walks all chunks of its column:
-// a second, partial wave would take as long as the first)
-constexpr int kDepth8 = 5, kBf16x8Threads = 64, kBf16x8MinCtas = 18;
+// bf16x8 kernel: 64-thread CTAs.  Each thread walks all chunks of its column, so the columns
+// must fit in one wave of evenly loaded SMs (a second, partial wave would take as long as the
+// first); within that, the ring of chunks in flight is as deep as the registers allow.  Layers
+// with many columns: depth 5 at <= 56 registers (18 CTAs per SM); few columns (long sequences,
+// small states): depth 16 (8 CTAs per SM) or 32 (4 CTAs per SM) keep enough bytes in flight
+// to cover the memory latency with a few hundred threads per SM.
+constexpr int kBf16x8Threads = 64;
 
 __device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
 __device__ __forceinline__ float4 load4(const float* src) { return __ldcs(reinterpret_cast<const float4*>(src)); }
@@ -42,8 +45,9 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// bf16 S / hprev, 8 elements per thread.
-__global__ void __launch_bounds__(kBf16x8Threads, kBf16x8MinCtas) state_passing_bf16x8_kernel(
+// bf16 S / hprev, 8 elements per thread, DEPTH chunks of S in flight.
+template <int DEPTH, int MIN_CTAS>
+__global__ void __launch_bounds__(kBf16x8Threads, MIN_CTAS) state_passing_bf16x8_kernel(
     const uint16_t* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     uint16_t* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN,
     int64_t nc, int64_t Q, int64_t total8) {
@@ -70,12 +74,12 @@ __global__ void __launch_bounds__(kBf16x8Threads, kBf16x8MinCtas) state_passing_
 #pragma unroll
     for (int i = 0; i < 8; ++i) hv[i] = 0.f;
   }
-  uint4 sbuf[kDepth8];
-  float dbuf[kDepth8];
+  uint4 sbuf[DEPTH];
+  float dbuf[DEPTH];
   const uint16_t* sp = S + (bi * nc * H + h) * PN + e;
   const float* dp = cs2 + bh * nc * Q + (Q - 1);
 #pragma unroll
-  for (int k = 0; k < kDepth8; ++k) {
+  for (int k = 0; k < DEPTH; ++k) {
     if (k < n) {
       sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
       dbuf[k] = __ldg(dp);
@@ -83,9 +87,9 @@ __global__ void __launch_bounds__(kBf16x8Threads, kBf16x8MinCtas) state_passing_
       dp += Q;
     }
   }
-  for (int c0 = 0; c0 < n; c0 += kDepth8) {
+  for (int c0 = 0; c0 < n; c0 += DEPTH) {
 #pragma unroll
-    for (int k = 0; k < kDepth8; ++k) {
+    for (int k = 0; k < DEPTH; ++k) {
       const int c = c0 + k;
       if (c < n) {
         uint4 o;
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(kBf16x8Threads, kBf16x8MinCtas) state_passing_
         hv[5] = fmaf(d, hv[5], bf16hi_to_f32(sbuf[k].z));
         hv[6] = fmaf(d, hv[6], bf16lo_to_f32(sbuf[k].w));
         hv[7] = fmaf(d, hv[7], bf16hi_to_f32(sbuf[k].w));
-        if (c + kDepth8 < n) {  // refill this ring entry with chunk c + kDepth8
+        if (c + DEPTH < n) {  // refill this ring entry with chunk c + DEPTH
           sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
           dbuf[k] = __ldg(dp);
           sp += cstride;
@@ -220,9 +224,19 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
   if (p.io_bf16 && PN % 8 == 0) {
     const int64_t total8 = p.b * p.H * (PN / 8);
     const unsigned blocks8 = static_cast<unsigned>((total8 + kBf16x8Threads - 1) / kBf16x8Threads);
-    return launch_pdl(state_passing_bf16x8_kernel, dim3(blocks8), dim3(kBf16x8Threads), 0, st,
-                      static_cast<const uint16_t*>(S), cs2, init, static_cast<uint16_t*>(hprev),
-                      final_state, p.H, PN, p.nc, p.Q, total8);
+    int sms = num_sms_current_device();
+    if (sms <= 0) sms = 1;
+    const int64_t ctas_per_sm = (int64_t(blocks8) + sms - 1) / sms;
+    const auto Sb = static_cast<const uint16_t*>(S);
+    const auto hb = static_cast<uint16_t*>(hprev);
+    if (ctas_per_sm <= 4)
+      return launch_pdl(state_passing_bf16x8_kernel<32, 4>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
+                        init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
+    if (ctas_per_sm <= 8)
+      return launch_pdl(state_passing_bf16x8_kernel<16, 8>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
+                        init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
+    return launch_pdl(state_passing_bf16x8_kernel<5, 18>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
+                      init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
   }
   const bool vec = (PN % 4) == 0;
   const int64_t total = p.b * p.H * (vec ? PN / 4 : PN);
