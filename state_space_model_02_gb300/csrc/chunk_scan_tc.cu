@@ -165,8 +165,11 @@ __device__ __forceinline__ void mask_block(const uint32_t (&v)[32], const float*
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
       const int e = 8 * c4 + 2 * e2;
-      float w0 = __uint_as_float(v[e]) * f[2 * e2] * rowf;
-      float w1 = __uint_as_float(v[e + 1]) * f[2 * e2 + 1] * rowf;
+      // packed pair products (one f32x2 multiply per factor)
+      const float2 w = mul_f32x2(mul_f32x2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                           make_float2(f[2 * e2], f[2 * e2 + 1])),
+                                 make_float2(rowf, rowf));
+      float w0 = w.x, w1 = w.y;
       if (DIAG) {
         w0 = e > dr ? 0.f : (e == dr ? w0 + Dh : w0);
         w1 = e + 1 > dr ? 0.f : (e + 1 == dr ? w1 + Dh : w1);
