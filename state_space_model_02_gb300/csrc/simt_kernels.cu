@@ -104,14 +104,16 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
 // i >= j0, 0 for rows above the block) scales the block's partial sums, so no per-head
 // matrix is formed and no factor overflows.
 template <typename IO, typename HT>
-__global__ void __launch_bounds__(256) chunk_scan_simt_kernel(
+__global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const IO* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ cs2, const float* __restrict__ dtT,
     const HT* __restrict__ hprev, IO* __restrict__ y, int64_t L, int64_t H, int64_t P, int64_t N,
     int64_t G, int64_t Q, int64_t nc, int64_t head_split) {
   extern __shared__ __align__(16) float CBs[];  // [jmax][GS]
-  __shared__ __align__(16) float As[KT][TM];
-  __shared__ __align__(16) float Bs[KT][TM];
+  // padded rows: the C / B / hprev fills write a column k at a time (stride GS, not TM, keeps
+  // those transposing stores from all landing in one bank)
+  __shared__ __align__(16) float As[KT][GS];
+  __shared__ __align__(16) float Bs[KT][GS];
   __shared__ float cs_i[TM], e_i[TM];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int64_t i0 = int64_t(blockIdx.y) * TM;
@@ -242,30 +244,45 @@ cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void*
 cudaError_t launch_chunk_scan_simt(const Problem& p, const void* x, const void* B, const void* C,
                                    const float* D, const float* cs2, const float* dtT,
                                    const void* hprev, void* y, cudaStream_t st) {
-  // split a group's heads over CTAs only as far as needed to give every SM two CTAs
+  // split a group's heads over CTAs: more CTAs fill the SMs' resident slots, but a partial
+  // last wave costs as much as a full one and every CTA computes its own C.B^T
   const int64_t row_tiles = (p.Q + TM - 1) / TM, base = row_tiles * p.b * p.nc * p.G;
   int sms = num_sms_current_device();
   if (sms <= 0) sms = 1;
-  int64_t split = (2 * sms + base - 1) / base;
-  if (split > p.hpg) split = p.hpg;
-  if (split < 1) split = 1;
+  const size_t smem = static_cast<size_t>(p.Q) * GS * sizeof(float);
+  cudaError_t e;
+  const auto kb = chunk_scan_simt_kernel<uint16_t, uint16_t>;
+  const auto kf = chunk_scan_simt_kernel<float, float>;
+  e = cudaFuncSetAttribute(p.io_bf16 ? reinterpret_cast<const void*>(kb) : reinterpret_cast<const void*>(kf),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, p.io_bf16 ? reinterpret_cast<const void*>(kb) : reinterpret_cast<const void*>(kf), 256, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  // cost of a split s ~ waves x (heads per CTA + the CTA's own C.B^T)
+  const int64_t slots = int64_t(per_sm) * sms;
+  int64_t split = 1, best = -1;
+  for (int64_t s = 1; s <= p.hpg; ++s) {
+    const int64_t waves = (base * s + slots - 1) / slots;
+    const int64_t cost = waves * ((p.hpg + s - 1) / s + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      split = s;
+    }
+  }
   if (p.G * split > 65535) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(p.b * p.nc), static_cast<unsigned>(row_tiles),
                   static_cast<unsigned>(p.G * split));
-  const size_t smem = static_cast<size_t>(p.Q) * GS * sizeof(float);
-  cudaError_t e;
   if (p.io_bf16) {
-    auto k = chunk_scan_simt_kernel<uint16_t, uint16_t>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    auto k = kb;
     k<<<grid, 256, smem, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(B),
                                static_cast<const uint16_t*>(C), D, cs2, dtT,
                                static_cast<const uint16_t*>(hprev), static_cast<uint16_t*>(y), p.L,
                                p.H, p.P, p.N, p.G, p.Q, p.nc, split);
   } else {
-    auto k = chunk_scan_simt_kernel<float, float>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    auto k = kf;
     k<<<grid, 256, smem, st>>>(static_cast<const float*>(x), static_cast<const float*>(B),
                                static_cast<const float*>(C), D, cs2, dtT,
                                static_cast<const float*>(hprev), static_cast<float*>(y), p.L, p.H,
