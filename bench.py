@@ -129,12 +129,18 @@ def load_peaks():
 
 
 def source_digest(kernel):
+    """Digest of a kernel's source file with comments and whitespace removed: a profile stays
+    valid across comment edits and is dropped by any change to the code."""
     files = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state_tc.cu",
              "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu",
              "decode": "decode.cu", "selective_scan": "selective_scan.cu"}
     p = os.path.join(ROOT, "state_space_model_02_gb300", "csrc", files[kernel])
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(p) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = "".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 def profiled_traffic(kernel, workload):

@@ -16,7 +16,7 @@
 // 2^{cs2_i - cs2_j0} * (2^{cs2_j0 - cs2_j} dt_j): one exp2 per row per block plus a per-head
 // column table; every factor stays inside float32 range (|cs2| over 32 tokens <= 32*max|dt A|/ln2).
 //
-// Persistent CTAs (one per SM: 512 TMEM columns, ~214 KB shared memory, 14 warps) walk a
+// Persistent CTAs (one per SM: 512 TMEM columns, ~214 KB shared memory, 23 warps) walk a
 // contiguous range of (batch, chunk, m-tile, head) units, weighted 2 : 3 for the two m-tiles
 // of a 256-token chunk (their measured cost ratio); CB is recomputed when the range crosses to a new (batch, chunk, m-tile, group).  Warp
 // roles, synchronised through mbarriers so the kinds of work overlap across heads:
