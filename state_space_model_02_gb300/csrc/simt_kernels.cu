@@ -46,13 +46,13 @@ __device__ __forceinline__ void mma4x4(float (&acc)[4][4], const float4 a, const
 // grid: x = p-tile * n_tiles + n-tile, y = h, z = b * nc + c.  S tile (64 p x 64 n) =
 // sum over the chunk's tokens t of (w_t x[t, p]) B[t, n].
 template <typename IO>
-__global__ void __launch_bounds__(256) chunk_state_simt_kernel(
+__global__ void __launch_bounds__(256, 3) chunk_state_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const float* __restrict__ cs2,
     const float* __restrict__ dtT, IO* __restrict__ S, int64_t L, int64_t H, int64_t P,
     int64_t N, int64_t G, int64_t Q, int64_t nc) {
   __shared__ __align__(16) float As[KT][TM];  // As[k][p] = w x[t0 + k, p0 + p]
   __shared__ __align__(16) float Bs[KT][TM];  // Bs[k][n] = B[t0 + k, n0 + n]
-  __shared__ float wsm[KT];
+  __shared__ float wsm[256];                  // the chunk's decay weights (Q <= 256)
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int64_t n_tiles = (N + TM - 1) / TM;
   const int64_t p0 = (blockIdx.x / n_tiles) * TM, n0 = (blockIdx.x % n_tiles) * TM;
@@ -61,25 +61,36 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(
   const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
   const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
   const float last = csr[Q - 1];
-  float acc[4][4] = {};
-  for (int64_t t0 = 0; t0 < Q; t0 += KT) {
-    if (tid < KT) {
-      const int64_t tok = c * Q + t0 + tid;
-      wsm[tid] = tok < L ? ex2(last - csr[t0 + tid]) * dtr[t0 + tid] : 0.f;
-    }
-    __syncthreads();
-    for (int e = tid; e < KT * TM; e += 256) {
-      const int k = e / TM, col = e % TM;
+  for (int t = tid; t < Q; t += 256) wsm[t] = c * Q + t < L ? ex2(last - csr[t]) * dtr[t] : 0.f;
+  // the next tile's x and B values are loaded into registers while the current tile's
+  // products run; element e = tid + 256 i of a tile is (k = e / TM, col = e % TM)
+  constexpr int kPer = KT * TM / 256;
+  float xr[kPer], br[kPer];
+  auto load_tile = [&](int64_t t0) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + 256 * i, k = e / TM, col = e % TM;
       const int64_t tok = c * Q + t0 + k;
-      float xv = 0.f, bv = 0.f;
+      xr[i] = 0.f;
+      br[i] = 0.f;
       if (tok < L) {
-        if (p0 + col < P) xv = wsm[k] * ld_io(x, ((b * L + tok) * H + h) * P + p0 + col);
-        if (n0 + col < N) bv = ld_io(Bm, ((b * L + tok) * G + g) * N + n0 + col);
+        if (p0 + col < P) xr[i] = ld_io(x, ((b * L + tok) * H + h) * P + p0 + col);
+        if (n0 + col < N) br[i] = ld_io(Bm, ((b * L + tok) * G + g) * N + n0 + col);
       }
-      As[k][col] = xv;
-      Bs[k][col] = bv;
+    }
+  };
+  float acc[4][4] = {};
+  load_tile(0);
+  __syncthreads();  // weights ready
+  for (int64_t t0 = 0; t0 < Q; t0 += KT) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + 256 * i, k = e / TM, col = e % TM;
+      As[k][col] = wsm[t0 + k] * xr[i];
+      Bs[k][col] = br[i];
     }
     __syncthreads();
+    if (t0 + KT < Q) load_tile(t0 + KT);
 #pragma unroll
     for (int k = 0; k < KT; ++k)
       mma4x4(acc, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
