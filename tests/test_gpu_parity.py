@@ -120,6 +120,14 @@ def test_edge_shapes(shape, dtype):
     check_against_oracle(inp)
 
 
+def test_cumsum_32_head_tiles():
+    # H a multiple of 32 and enough chunks: chunk_cumsum stages 32 heads per CTA (whole
+    # 128-byte rows of dt); ragged last chunk
+    inp = synth.make_inputs(batch=1, seqlen=19520 + 37, nheads=32, headdim=16, dstate=16, chunk=64,
+                            io_dtype="f32", init=True, seed=17)
+    check_against_oracle(inp)
+
+
 def test_slow_decay_exercises_state_passing():
     # |A| in [0.001, 0.05]: the state carries across many chunks
     inp = synth.make_inputs(batch=1, seqlen=4096, nheads=4, headdim=64, dstate=128, chunk=256,
