@@ -275,6 +275,31 @@ def test_generator_is_deterministic_and_in_range():
     assert a.init is None
 
 
+def test_generator_distribution_matches_recipe():
+    # dt = clip(softplus(N(-3, 1)), 1e-3, 0.1): the clipped fractions are normal tail masses;
+    # A = -exp(U(0, ln 16)); x ~ N(0, 1), rounded to bf16
+    import math
+    inp = synth.make_inputs(batch=1, seqlen=2048, nheads=2048, headdim=2, dstate=2, chunk=256,
+                            io_dtype="bf16", seed=23)
+    dt = inp.dt.ravel()
+    n = dt.size
+
+    def tail_above(v):  # P(N(-3, 1) > v)
+        return 0.5 * math.erfc((v + 3.0) / math.sqrt(2.0))
+
+    p_hi = tail_above(math.log(math.expm1(0.1)))           # about 0.227
+    p_lo = 1.0 - tail_above(math.log(math.expm1(1e-3)))    # about 5e-5
+    f_hi = np.mean(dt == np.float32(0.1))
+    f_lo = np.mean(dt == np.float32(1e-3))
+    assert abs(f_hi - p_hi) < 5 * math.sqrt(p_hi * (1 - p_hi) / n)
+    assert abs(f_lo - p_lo) < 5 * math.sqrt(p_lo * (1 - p_lo) / n) + 1.0 / n
+    u = np.log(-inp.A.astype(np.float64)) / math.log(16.0)   # U(0, 1)
+    assert abs(u.mean() - 0.5) < 5 * math.sqrt(1.0 / 12.0 / u.size)
+    assert u.min() >= 0.0 and u.max() <= 1.0
+    x = synth.bf16_bits_to_f32(inp.x).astype(np.float64).ravel()
+    assert abs(x.mean()) < 5.0 / math.sqrt(x.size) and abs(x.std() - 1.0) < 0.01
+
+
 # ------------------------------------------------------------------------ mutations
 
 
