@@ -29,7 +29,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "mamba2_130m_layer"
+DEFAULT_WORKLOAD = "long_256k"
 METRIC = "SSD forward tokens/s on 1 GB300 + per-kernel % of HBM/tensor roofline"
 METRIC_DECODE = "SSD decode tokens/s on 1 GB300 + % of HBM roofline"
 

@@ -31,6 +31,13 @@
  *     ABI.  Argument checks happen on the host before any launch; a failed
  *     check launches nothing.  ssd_last_error() gives a one-line detail of the
  *     last failure on the calling thread.
+ *   - Step sizes and decay rates: any finite dt >= 0 and A <= 0 (a state that
+ *     decays, as in the method), of any magnitude.  The chunked kernels split
+ *     each decay weight exp(sum of dt A) into factors that stay inside float32
+ *     range for every such input (a chunk's rows whose own 32-token block decays
+ *     too steeply for that take per-element exponentials).  Growing states
+ *     (dt * A > 0) are computed by the same arithmetic and are exact only while
+ *     every weight of a chunk stays inside float32 range.
  *   - Kernels that wait on on-chip barriers give every wait a time limit; on
  *     expiry they record SSD_ERR_TIMEOUT in the workspace status word, drain
  *     their own copies, release tensor memory and return.  ssd_read_status()
@@ -163,7 +170,10 @@ ssd_status ssd_selftest_wait_timeout(uint32_t* status_word, uint64_t timeout_ns,
  *     rejected with SSD_ERR_WORKSPACE before anything is launched.
  *   - The first call on a device (with that device current) looks up the array's device
  *     address with cudaGetSymbolAddress and caches it; make that first call before any
- *     stream capture on the device.
+ *     stream capture on the device.  The cache is not refreshed: after cudaDeviceReset
+ *     the library must be reloaded before this entry point is used again.
+ *   - `stream` must belong to the current device; a stream of another device is rejected
+ *     with SSD_ERR_INVALID before anything is launched.
  *   - Every call on a device shares the one array, which keeps the previous call's
  *     intermediates: calls whose work overlaps on the GPU (other streams, other threads)
  *     race on it and must be ordered by the caller.

@@ -67,8 +67,11 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
     float* out_cs = cs2 + ((b * H + h) * nc + c) * Q;
     float* out_dt = dtT + ((b * H + h) * nc + c) * Q;
     // round r covers tokens 32r .. 32r+31, one per lane: a warp-shuffle inclusive scan plus the
-    // running total of the earlier rounds; every store is one coalesced 128-byte row
-    float carry = 0.f;
+    // running total of the earlier rounds; every store is one coalesced 128-byte row.  Tokens
+    // past the sequence end repeat the last token's value bit for bit: each lane's prefix comes
+    // from its own tree of additions, so summing the padding's zeros would not reproduce it, and
+    // the chunk-end value is the reference every decay of the chunk is taken against.
+    float carry = 0.f, last = 0.f;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int t = 32 * r + lane;
@@ -79,7 +82,14 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
         const float o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
       }
-      out_cs[t] = (carry + incl) * kLog2e;
+      float v = (carry + incl) * kLog2e;
+      const int64_t valid = L - (c * Q + 32 * r);  // tokens of this round inside the sequence
+      if (valid < 32) {                            // uniform over the warp
+        const float lastv = __shfl_sync(0xffffffffu, v, valid > 0 ? int(valid) - 1 : 0);
+        if (lane >= valid) v = valid > 0 ? lastv : last;
+      }
+      last = __shfl_sync(0xffffffffu, v, 31);
+      out_cs[t] = v;
       out_dt[t] = unit_scale ? (c * Q + t < L ? 1.f : 0.f) : d;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }

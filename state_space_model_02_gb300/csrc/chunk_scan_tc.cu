@@ -12,9 +12,13 @@
 // with P = L o CB + D_h I: CB never leaves TMEM; for every head it is read back into registers,
 // multiplied by the decay mask L_ij = 2^{cs2_i - cs2_j} dt_j (j <= i, else 0), D_h is added on
 // the diagonal (so Y1 already holds D_h x_i), and the result is rounded to bf16 into shared
-// memory as Y1's A operand.  The mask is factored per 32-column block j0 as
-// 2^{cs2_i - cs2_j0} * (2^{cs2_j0 - cs2_j} dt_j): one exp2 per row per block plus a per-head
-// column table; every factor stays inside float32 range (|cs2| over 32 tokens <= 32*max|dt A|/ln2).
+// memory as Y1's A operand.  The mask is factored per 32-column block [j0, j1], j1 = j0 + 31, as
+// 2^{cs2_i - cs2_j1} * (2^{cs2_j1 - cs2_j} dt_j): one exp2 per row per block plus a per-head
+// column table.  With decaying steps (dt A <= 0, cs2 non-increasing) both factors of a block
+// left of the row's own are <= 1, whatever the step sizes, so they can only underflow where the
+// weight itself is negligible.  In the row's own (diagonal) block the row factor grows with
+// the block's decay span cs2_j0 - cs2_j1; where that span exceeds kMaxFactorSpan (log2 units)
+// the block takes every weight as one exp2 per element instead.
 //
 // Persistent CTAs (one per SM: 512 TMEM columns, ~214 KB shared memory, 23 warps) walk a
 // contiguous range of (batch, chunk, m-tile, head) units, weighted 2 : 3 for the two m-tiles
@@ -52,6 +56,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kBox128 = 16384;  // TMA box: 128 rows x 128 bytes
 constexpr uint32_t kBox64 = 8192;    // TMA box: 64 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;  // CB [0,256) | Y1 buf0 | Y2 buf0 | Y1 buf1 | Y2 buf1
+// Largest |cs2_j0 - cs2_j1| (log2 units) of a diagonal block for which the factored weights are
+// used: each factor then stays within 2^{+-64}, far inside float32's range.
+constexpr float kMaxFactorSpan = 64.f;
 // named barriers: the mask group, the epilogue group, and the poller -> MMA issuer handoff
 constexpr uint32_t kBarMask = 1, kBarEpi = 2, kBarIssue = 3;
 
@@ -175,6 +182,29 @@ __device__ __forceinline__ void mask_block(const uint32_t (&v)[32], const float*
         w1 = e + 1 > dr ? 0.f : (e + 1 == dr ? w1 + Dh : w1);
       }
       o[e2] = pack_bf16x2(w0, w1);
+    }
+    *reinterpret_cast<uint4*>(pb + (((cbase + c4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// The diagonal block of a row whose block decays by more than kMaxFactorSpan: every weight
+// 2^{cs2_i - cs2_j} dt_j (j <= i) is one exp2 of its own, so no factor leaves float32's range.
+// csb / dtb: the block's cs2 and dt values (shared memory, the same for every lane).
+__device__ __forceinline__ void mask_block_exact(const uint32_t (&v)[32], const float* csb, const float* dtb,
+                                                 float cs_i, int dr, float Dh, uint8_t* pb, int cbase, int r) {
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    uint32_t o[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int e = 8 * c4 + 2 * e2;
+      float w[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float wt = e + u > dr ? 0.f : ex2(cs_i - csb[e + u]) * dtb[e + u];
+        w[u] = __uint_as_float(v[e + u]) * wt + (e + u == dr ? Dh : 0.f);
+      }
+      o[e2] = pack_bf16x2(w[0], w[1]);
     }
     *reinterpret_cast<uint4*>(pb + (((cbase + c4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -447,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* colf = reinterpret_cast<float*>(smem + SM::kColf + (gi & 1) * 1024);
         const bool have = mbar_wait(bar(kXsFull0 + s), (gi >> 1) & 1, ctl);
         if (have && mt_thread < jrows)
-          colf[mt_thread] = ex2(cs[mt_thread & ~31] - cs[mt_thread]) * dtv[mt_thread];
+          colf[mt_thread] = ex2(cs[mt_thread | 31] - cs[mt_thread]) * dtv[mt_thread];
         const float cs_i = have ? cs[row] : 0.f;
         const float Dh = prm.D ? __ldg(prm.D + sg.h_begin + hi) : 0.f;
         named_bar_sync(kBarMask, 32 * kMaskWarps);
@@ -473,17 +503,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                              mbar_wait(bar(kPEmpty0 + k), ((gpar >> k) & 1u) ^ 1u, ctl);
           if (mine) tmem_ld_wait();
           if (mine && pfree) {
-            // P[row, j] = CB[row, j] colf[j] 2^(cs2_row - cs2_j0), zero right of the diagonal,
+            // P[row, j] = CB[row, j] colf[j] 2^(cs2_row - cs2_j1), zero right of the diagonal,
             // plus D_h on it
-            const float rowf = ex2(cs_i - cs[j0]);
+            const float rowf = ex2(cs_i - cs[j0 + 31]);
             const float* cf = colf + j0;
             uint8_t* pb = smem + SM::kP + (j0 >> 6) * kBox128 + r * 128;
             const int cbase = (j0 & 63) >> 3;
-            // one branch per block: the diagonal block masks j > row and adds D_h on j == row
-            if (blk == maxblk)
+            // one branch per block (uniform across the warp): the diagonal block masks j > row and
+            // adds D_h on j == row, per element when its decay span is too wide to factor
+            if (blk != maxblk)
+              mask_block<false>(v, cf, rowf, 0, 0.f, pb, cbase, r);
+            else if (fabsf(cs[j0] - cs[j0 + 31]) <= kMaxFactorSpan)
               mask_block<true>(v, cf, rowf, row - j0, Dh, pb, cbase, r);
             else
-              mask_block<false>(v, cf, rowf, 0, 0.f, pb, cbase, r);
+              mask_block_exact(v, cs + j0, dtv + j0, cs_i, row - j0, Dh, pb, cbase, r);
           }
           fence_proxy_async_smem();
           __syncwarp();

@@ -30,9 +30,14 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-ssd_status scratch_for_current_device(void** out) {
+ssd_status scratch_for_current_device(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  // the cached address belongs to the current device: a stream of another device would run
+  // the kernels there with a pointer into this device's array
+  int stream_dev = -1;
+  if (cudaStreamGetDevice(stream, &stream_dev) != cudaSuccess) return SSD_ERR_CUDA;
+  if (stream_dev != dev) return SSD_ERR_INVALID;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
@@ -52,7 +57,7 @@ ssd_status ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const float* d
                            const void* B, const void* C, const float* D, const float* init_state,
                            void* y, float* final_state, void* stream) {
   void* scratch = nullptr;
-  const ssd_status s = scratch_for_current_device(&scratch);
+  const ssd_status s = scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (s != SSD_OK) return s;
   // ssd_fwd checks the shape's scratch need against the array's size before it launches
   // anything, and returns SSD_ERR_WORKSPACE when the shape needs more.

@@ -34,6 +34,7 @@ __device__ __forceinline__ void st_io(uint16_t* p, int64_t i, float v) {
 constexpr int TM = 64;  // tile edge
 constexpr int KT = 16;  // k values staged per step
 constexpr int GS = TM + 4;  // row stride of the masked-matrix buffer (keeps float4 alignment)
+constexpr float kMaxFactorSpan = 64.f;  // widest factored decay span inside a diagonal block
 
 __device__ __forceinline__ void mma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
   const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -110,10 +111,12 @@ __global__ void __launch_bounds__(256, 3) chunk_state_simt_kernel(
 // CTA computes the tile's causal C_i . B_j (j <= i, j < jmax) once -- it is the same for every
 // head of the group -- into dynamic shared memory, transposed (CBs[j][i]), then runs the heads
 // [part * per, (part + 1) * per) of the group.  Per head the decay 2^{cs2_i - cs2_j} dt_j is
-// applied in blocks of KT columns j starting at j0: 2^{cs2_j0 - cs2_j} dt_j (>= 0, at most
-// 2^{KT max|dt A| log2 e}) scales the staged x rows and 2^{cs2_i - cs2_j0} (<= 1 for
-// i >= j0, 0 for rows above the block) scales the block's partial sums, so no per-head
-// matrix is formed and no factor overflows.
+// applied in blocks of KT columns [j0, j1], j1 = j0 + KT - 1: 2^{cs2_j1 - cs2_j} dt_j scales the
+// staged x rows and 2^{cs2_i - cs2_j1} (0 for rows above the block) scales the block's partial
+// sums, so no per-head matrix is formed.  With decaying steps (dt A <= 0) both factors are
+// <= 1 for every row i >= j1, whatever the step sizes; only rows inside the block see a row
+// factor above 1, bounded by 2^{cs2_j0 - cs2_j1}.  A block that holds such rows and decays by
+// more than kMaxFactorSpan (log2 units) takes each weight as one exp2 of its own instead.
 template <typename IO, typename HT>
 __global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const IO* __restrict__ Cm,
@@ -178,27 +181,49 @@ __global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
     for (int64_t p0 = 0; p0 < P; p0 += TM) {
       float acc1[4][4] = {}, acc2[4][4] = {};
       for (int64_t j0 = 0; j0 < jmax; j0 += KT) {
-        const float cj0 = csr[j0];
+        const float cj1 = csr[j0 + KT - 1];
+        // uniform over the CTA: a block left of every row of the tile (j0 < i0) always factors
+        const bool factored = j0 < i0 || fabsf(csr[j0] - cj1) <= kMaxFactorSpan;
         for (int e = tid; e < KT * TM; e += 256) {
           const int k = e / TM, col = e % TM;
           const int64_t tj = j0 + k;
           float v = 0.f;
           if (row_ok(tj) && p0 + col < P)
-            v = ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) * (ex2(cj0 - csr[tj]) * dtr[tj]);
+            v = ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) *
+                (factored ? ex2(cj1 - csr[tj]) * dtr[tj] : dtr[tj]);
           Bs[k][col] = v;
         }
         __syncthreads();
-        float part_acc[4][4] = {};
+        if (factored) {
+          float part_acc[4][4] = {};
 #pragma unroll
-        for (int k = 0; k < KT; ++k)
-          mma4x4(part_acc, *reinterpret_cast<const float4*>(&CBs[(j0 + k) * GS + 4 * ty]),
-                 *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+          for (int k = 0; k < KT; ++k)
+            mma4x4(part_acc, *reinterpret_cast<const float4*>(&CBs[(j0 + k) * GS + 4 * ty]),
+                   *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int il = 4 * ty + r;
-          const float rf = (j0 <= i0 + il) ? ex2(cs_i[il] - cj0) : 0.f;
+          for (int r = 0; r < 4; ++r) {
+            const int il = 4 * ty + r;
+            const float rf = (j0 <= i0 + il) ? ex2(cs_i[il] - cj1) : 0.f;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(rf, part_acc[r][cc], acc1[r][cc]);
+            for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(rf, part_acc[r][cc], acc1[r][cc]);
+          }
+        } else {
+          // every weight 2^{cs2_i - cs2_j} (j <= i) on its own; CBs is already zero for j > i
+#pragma unroll 4
+          for (int k = 0; k < KT; ++k) {
+            const int64_t j = j0 + k;
+            const float cjk = csr[j];
+            const float4 cb = *reinterpret_cast<const float4*>(&CBs[j * GS + 4 * ty]);
+            const float4 xv = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
+            const float cbv[4] = {cb.x, cb.y, cb.z, cb.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int il = 4 * ty + r;
+              const float a = j <= i0 + il ? cbv[r] * ex2(cs_i[il] - cjk) : 0.f;
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(a, xw[cc], acc1[r][cc]);
+            }
+          }
         }
         __syncthreads();
       }

@@ -80,8 +80,12 @@ def bf16_bits_to_f32(a: np.ndarray) -> np.ndarray:
 
 
 def make_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, chunk=256, io_dtype="bf16",
-                init=False, seed=0, a_range=(1.0, 16.0), with_D=True) -> SSDInputs:
-    """Draw one problem from the distributions in the module docstring."""
+                init=False, seed=0, a_range=(1.0, 16.0), with_D=True, dt_mean=-3.0,
+                dt_clip=(1e-3, 0.1)) -> SSDInputs:
+    """Draw one problem from the distributions in the module docstring.
+
+    dt_mean and dt_clip move the step-size distribution (softplus(N(dt_mean, 1)) clipped to
+    dt_clip) for the large-step edge cases; the defaults are the workloads' recipe."""
     if io_dtype not in ("bf16", "f32"):
         raise ValueError("io_dtype must be 'bf16' or 'f32'")
     rng = np.random.default_rng(seed)
@@ -89,16 +93,17 @@ def make_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, chunk=256, io
     x = rng.standard_normal((b, L, H, P), dtype=np.float32)
     Bm = rng.standard_normal((b, L, G, N), dtype=np.float32)
     Cm = rng.standard_normal((b, L, G, N), dtype=np.float32)
-    dt_raw = rng.normal(-3.0, 1.0, size=(b, L, H))
+    dt_raw = rng.normal(dt_mean, 1.0, size=(b, L, H))
     a_u = rng.uniform(np.log(a_range[0]), np.log(a_range[1]), size=H)
     D = rng.standard_normal(H).astype(np.float32)
     h0 = rng.normal(0.0, 0.1, size=(b, H, P, N)).astype(np.float32) if init else None
-    dt = np.clip(np.logaddexp(0.0, dt_raw), 1e-3, 0.1).astype(np.float32)
+    dt = np.clip(np.logaddexp(0.0, dt_raw), dt_clip[0], dt_clip[1]).astype(np.float32)
     A = (-np.exp(a_u)).astype(np.float32)
     if io_dtype == "bf16":
         x, Bm, Cm = to_bf16_bits(x), to_bf16_bits(Bm), to_bf16_bits(Cm)
     return SSDInputs(x=x, dt=dt, A=A, B=Bm, C=Cm, D=D if with_D else None, init=h0, chunk=chunk,
-                     io_dtype=io_dtype, meta=dict(seed=seed, a_range=tuple(a_range)))
+                     io_dtype=io_dtype, meta=dict(seed=seed, a_range=tuple(a_range), dt_mean=dt_mean,
+                                                  dt_clip=tuple(dt_clip)))
 
 
 def make_config(name: str, seed: int = 0, **overrides) -> SSDInputs:

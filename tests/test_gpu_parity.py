@@ -135,6 +135,63 @@ def test_slow_decay_exercises_state_passing():
     check_against_oracle(inp)
 
 
+# ---------------------------------------------------------------- large steps
+#
+# The recurrence holds for any positive step and negative A; the kernels factor each decay
+# weight 2^{cs2_i - cs2_j} dt_j into per-row and per-column parts, which must stay inside
+# float32's range however fast the state decays.  dt in [0.5, 2] with A = -16 decays by
+# 2^-11.5 .. 2^-46 per token (hundreds of log2 units per 32-token block); dt in [0.05, 0.3]
+# with A = -4 puts a block's decay span around the point where the diagonal block switches
+# from factored to per-element weights.
+
+BIG_STEPS = dict(dt_mean=0.5, dt_clip=(0.5, 2.0), a_range=(16.0, 16.0))
+MID_STEPS = dict(dt_mean=-2.0, dt_clip=(0.05, 0.3), a_range=(4.0, 4.0))
+
+
+@pytest.mark.parametrize("steps", [BIG_STEPS, MID_STEPS], ids=["big", "mid"])
+@pytest.mark.parametrize("shape", [
+    dict(batch=1, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk=256),   # tensor-core scan
+    dict(batch=1, seqlen=700, nheads=3, headdim=64, dstate=256, chunk=256),    # two state slices
+    dict(batch=1, seqlen=600, nheads=2, headdim=64, dstate=128, chunk=128),
+    dict(batch=1, seqlen=520, nheads=3, headdim=64, dstate=128, chunk=64),     # CUDA-core scan
+], ids=["q256n128", "q256n256", "q128n128", "q64n128"])
+def test_large_steps_bf16(shape, steps):
+    inp = synth.make_inputs(io_dtype="bf16", init=True, seed=21, **shape, **steps)
+    check_against_oracle(inp)
+
+
+@pytest.mark.parametrize("steps", [BIG_STEPS, MID_STEPS], ids=["big", "mid"])
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_large_steps_f32_cuda_cores(chunk, steps):
+    inp = synth.make_inputs(batch=1, seqlen=600, nheads=3, headdim=32, dstate=64, chunk=chunk,
+                            io_dtype="f32", init=True, seed=22, **steps)
+    check_against_oracle(inp)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_large_steps_forced_onto_cuda_cores(dtype):
+    inp = synth.make_inputs(batch=1, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk=256,
+                            io_dtype=dtype, init=True, seed=23, **BIG_STEPS)
+    check_against_oracle(inp, flags=ssd.FLAG_FORCE_SIMT)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_one_head_with_large_steps_among_small(dtype):
+    # heads 0, 1, 3 keep the workloads' steps; head 2 takes steps in [0.5, 2] with A = -16
+    inp = synth.make_inputs(batch=2, seqlen=900, nheads=4, headdim=64, dstate=128, chunk=256,
+                            io_dtype=dtype, init=True, seed=24)
+    big = synth.make_inputs(batch=2, seqlen=900, nheads=4, headdim=64, dstate=128, chunk=256,
+                            io_dtype=dtype, init=True, seed=25, **BIG_STEPS)
+    inp.dt[:, :, 2] = big.dt[:, :, 2]
+    inp.A[2] = big.A[2]
+    check_against_oracle(inp)
+    # the heads with ordinary steps are held to the tolerance on their own
+    y, _ = run(inp)
+    pairs = [(b, h) for b in range(2) for h in (0, 1, 3)]
+    out = oracle_pairs(inp, pairs)
+    assert rel(gather_y(y, pairs), out["y"]) <= TOL[dtype]
+
+
 def test_no_D_and_no_init():
     inp = synth.make_inputs(batch=1, seqlen=512, nheads=4, headdim=64, dstate=128, chunk=256,
                             io_dtype="bf16", init=False, seed=7, with_D=False)
