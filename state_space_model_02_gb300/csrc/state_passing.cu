@@ -11,21 +11,26 @@
 //
 // The loop over chunks is a dependent FMA chain per element, so the kernel is bound by HBM
 // latency x bandwidth: each thread owns consecutive state elements -- 8 (one 16-byte load of S
-// per chunk) when S is bf16, 4 when it is float32 -- and keeps kDepth chunks of S in flight in
-// registers ahead of the chain.  The chain itself runs in float32.
+// per chunk) when S is bf16, 4 when it is float32 -- and loads the chunks in batches of K: all K
+// loads of a batch are issued together (with the next batch's issued before this one is
+// consumed, where registers allow), then the K chain steps run.  A ring that refills one entry
+// per chunk keeps as many loads in flight on paper, but a warp tracks its outstanding loads in a
+// handful of dependency counters, so waiting for the oldest entry of the ring also waits for
+// loads issued just before it: measured on GB300 at 256K tokens, rings of 8 to 32 chunks all ran
+// at 1.9 TB/s, batches of 16 at 6.5 TB/s (a plain copy of the same bytes: 6.5 TB/s).
+// The chain itself runs in float32.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
 namespace {
 
-constexpr int kDepth = 8;
+constexpr int kVec4Batch = 8;
 // bf16x8 kernel: 64-thread CTAs.  Each thread walks all chunks of its column, so the columns
 // must fit in one wave of evenly loaded SMs (a second, partial wave would take as long as the
-// first); within that, the ring of chunks in flight is as deep as the registers allow.  Layers
-// with many columns: depth 5 at <= 56 registers (18 CTAs per SM); few columns (long sequences,
-// small states): depth 16 (8 CTAs per SM) or 32 (4 CTAs per SM) keep enough bytes in flight
-// to cover the memory latency with a few hundred threads per SM.
+// first); within that, the batch is as large as the registers allow.  Few columns (long
+// sequences, small states): batches of 16 with the next batch in flight (<= 4 CTAs per SM);
+// layers: batches of 8 (<= 12 CTAs per SM) or 4 (<= 18 CTAs per SM).
 constexpr int kBf16x8Threads = 64;
 
 __device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
@@ -45,8 +50,9 @@ __device__ __forceinline__ void store4(uint16_t* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// bf16 S / hprev, 8 elements per thread, DEPTH chunks of S in flight.
-template <int DEPTH, int MIN_CTAS>
+// bf16 S / hprev, 8 elements per thread, chunks in batches of K (PF: the next batch's loads are
+// issued before the current batch is consumed).
+template <int K, bool PF, int MIN_CTAS>
 __global__ void __launch_bounds__(kBf16x8Threads, MIN_CTAS) state_passing_bf16x8_kernel(
     const uint16_t* __restrict__ S, const float* __restrict__ cs2, const float* __restrict__ init,
     uint16_t* __restrict__ hprev, float* __restrict__ final_state, int64_t H, int64_t PN,
@@ -62,6 +68,8 @@ __global__ void __launch_bounds__(kBf16x8Threads, MIN_CTAS) state_passing_bf16x8
   const int64_t bi = bh / H, h = bh % H;
   const int64_t cstride = H * PN;  // elements between chunks in S / hprev
   uint16_t* Hp = hprev + (bi * nc * H + h) * PN + e;
+  const uint16_t* Sp = S + (bi * nc * H + h) * PN + e;
+  const float* dp = cs2 + bh * nc * Q + (Q - 1);
   const int n = static_cast<int>(nc);
 
   float hv[8];
@@ -74,22 +82,34 @@ __global__ void __launch_bounds__(kBf16x8Threads, MIN_CTAS) state_passing_bf16x8
 #pragma unroll
     for (int i = 0; i < 8; ++i) hv[i] = 0.f;
   }
-  uint4 sbuf[DEPTH];
-  float dbuf[DEPTH];
-  const uint16_t* sp = S + (bi * nc * H + h) * PN + e;
-  const float* dp = cs2 + bh * nc * Q + (Q - 1);
+  uint4 sb[K], nb[K];
+  float db[K], nd[K];
+  // Sp / dp always point at the next chunk to load
+  auto load_batch = [&](uint4 (&sv)[K], float (&dv)[K], int c0) {
 #pragma unroll
-  for (int k = 0; k < DEPTH; ++k) {
-    if (k < n) {
-      sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
-      dbuf[k] = __ldg(dp);
-      sp += cstride;
-      dp += Q;
+    for (int k = 0; k < K; ++k) {
+      if (c0 + k < n) {
+        sv[k] = __ldcs(reinterpret_cast<const uint4*>(Sp));
+        dv[k] = __ldg(dp);
+        Sp += cstride;
+        dp += Q;
+      }
     }
-  }
-  for (int c0 = 0; c0 < n; c0 += DEPTH) {
+  };
+  if (PF) load_batch(nb, nd, 0);
+  for (int c0 = 0; c0 < n; c0 += K) {
+    if (PF) {
 #pragma unroll
-    for (int k = 0; k < DEPTH; ++k) {
+      for (int k = 0; k < K; ++k) {
+        sb[k] = nb[k];
+        db[k] = nd[k];
+      }
+      if (c0 + K < n) load_batch(nb, nd, c0 + K);
+    } else {
+      load_batch(sb, db, c0);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
       const int c = c0 + k;
       if (c < n) {
         uint4 o;
@@ -99,21 +119,15 @@ __global__ void __launch_bounds__(kBf16x8Threads, MIN_CTAS) state_passing_bf16x8
         o.w = pack_bf16x2(hv[6], hv[7]);
         *reinterpret_cast<uint4*>(Hp) = o;
         Hp += cstride;
-        const float d = ex2(dbuf[k]);
-        hv[0] = fmaf(d, hv[0], bf16lo_to_f32(sbuf[k].x));
-        hv[1] = fmaf(d, hv[1], bf16hi_to_f32(sbuf[k].x));
-        hv[2] = fmaf(d, hv[2], bf16lo_to_f32(sbuf[k].y));
-        hv[3] = fmaf(d, hv[3], bf16hi_to_f32(sbuf[k].y));
-        hv[4] = fmaf(d, hv[4], bf16lo_to_f32(sbuf[k].z));
-        hv[5] = fmaf(d, hv[5], bf16hi_to_f32(sbuf[k].z));
-        hv[6] = fmaf(d, hv[6], bf16lo_to_f32(sbuf[k].w));
-        hv[7] = fmaf(d, hv[7], bf16hi_to_f32(sbuf[k].w));
-        if (c + DEPTH < n) {  // refill this ring entry with chunk c + DEPTH
-          sbuf[k] = __ldcs(reinterpret_cast<const uint4*>(sp));
-          dbuf[k] = __ldg(dp);
-          sp += cstride;
-          dp += Q;
-        }
+        const float d = ex2(db[k]);
+        hv[0] = fmaf(d, hv[0], bf16lo_to_f32(sb[k].x));
+        hv[1] = fmaf(d, hv[1], bf16hi_to_f32(sb[k].x));
+        hv[2] = fmaf(d, hv[2], bf16lo_to_f32(sb[k].y));
+        hv[3] = fmaf(d, hv[3], bf16hi_to_f32(sb[k].y));
+        hv[4] = fmaf(d, hv[4], bf16lo_to_f32(sb[k].z));
+        hv[5] = fmaf(d, hv[5], bf16hi_to_f32(sb[k].z));
+        hv[6] = fmaf(d, hv[6], bf16lo_to_f32(sb[k].w));
+        hv[7] = fmaf(d, hv[7], bf16hi_to_f32(sb[k].w));
       }
     }
   }
@@ -144,25 +158,24 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
 
   float4 hv = init ? __ldg(reinterpret_cast<const float4*>(init + bh * PN + e))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 sbuf[kDepth];
-  float dbuf[kDepth];
-  // prologue: the first kDepth chunks in flight; pointers advance one chunk per load
+  float4 sbuf[kVec4Batch];
+  float dbuf[kVec4Batch];
   const HT* sp = S + (bi * nc * H + h) * PN + e;
   const float* dp = cs2 + bh * nc * Q + (Q - 1);
+  for (int c0 = 0; c0 < n; c0 += kVec4Batch) {
+    // one batch of loads in flight together, then its chain steps
 #pragma unroll
-  for (int k = 0; k < kDepth; ++k) {
-    if (k < n) {
-      sbuf[k] = load4(sp);
-      dbuf[k] = __ldg(dp);
-      sp += cstride;
-      dp += Q;
+    for (int k = 0; k < kVec4Batch; ++k) {
+      if (c0 + k < n) {
+        sbuf[k] = load4(sp);
+        dbuf[k] = __ldg(dp);
+        sp += cstride;
+        dp += Q;
+      }
     }
-  }
-  for (int c0 = 0; c0 < n; c0 += kDepth) {
 #pragma unroll
-    for (int k = 0; k < kDepth; ++k) {
-      const int c = c0 + k;
-      if (c < n) {
+    for (int k = 0; k < kVec4Batch; ++k) {
+      if (c0 + k < n) {
         store4(Hp, hv);
         Hp += cstride;
         const float d = ex2(dbuf[k]);
@@ -170,12 +183,6 @@ __global__ void __launch_bounds__(256, 4) state_passing_vec4_kernel(
         hv.y = fmaf(d, hv.y, sbuf[k].y);
         hv.z = fmaf(d, hv.z, sbuf[k].z);
         hv.w = fmaf(d, hv.w, sbuf[k].w);
-        if (c + kDepth < n) {  // refill this ring entry with chunk c + kDepth
-          sbuf[k] = load4(sp);
-          dbuf[k] = __ldg(dp);
-          sp += cstride;
-          dp += Q;
-        }
       }
     }
   }
@@ -230,13 +237,13 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
     const auto Sb = static_cast<const uint16_t*>(S);
     const auto hb = static_cast<uint16_t*>(hprev);
     if (ctas_per_sm <= 4)
-      return launch_pdl(state_passing_bf16x8_kernel<32, 4>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
-                        init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
-    if (ctas_per_sm <= 8)
-      return launch_pdl(state_passing_bf16x8_kernel<16, 8>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
-                        init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
-    return launch_pdl(state_passing_bf16x8_kernel<5, 18>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb, cs2,
-                      init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
+      return launch_pdl(state_passing_bf16x8_kernel<16, true, 4>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+                        cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
+    if (ctas_per_sm <= 12)
+      return launch_pdl(state_passing_bf16x8_kernel<8, false, 12>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+                        cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
+    return launch_pdl(state_passing_bf16x8_kernel<4, false, 18>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+                      cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
   }
   const bool vec = (PN % 4) == 0;
   const int64_t total = p.b * p.H * (vec ? PN / 4 : PN);
