@@ -109,7 +109,8 @@ struct ScSmem {
   static constexpr int kNumBars = 26;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kUsed = kAbort + 4;
+  static constexpr uint32_t kWalk = kAbort + 4;              // SegWalk of the CTA's first unit
+  static constexpr uint32_t kUsed = kWalk + 32;
   static constexpr uint32_t kAlloc = kUsed + 1024;           // slack for 1024-byte alignment
   static_assert(kXsBytes % 1024 == 0 && kHpBytes % 1024 == 0, "slots must stay 1024-byte aligned");
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
@@ -143,18 +144,50 @@ struct Segment {
   int b, c, mt, g, h_begin, nh;
 };
 
-__device__ __forceinline__ Segment segment_at(int64_t u, int64_t u_end, const ScParams& prm) {
-  Segment s;
-  const int64_t bcm = u / prm.H;
-  s.h_begin = static_cast<int>(u % prm.H);
-  s.mt = static_cast<int>(bcm % prm.MT);
-  const int64_t bc = bcm / prm.MT;
-  s.c = static_cast<int>(bc % prm.nc);
-  s.b = static_cast<int>(bc / prm.nc);
-  s.g = s.h_begin / prm.hpg;
-  const int64_t h_end = min(int64_t((s.g + 1) * prm.hpg), s.h_begin + (u_end - u));
-  s.nh = static_cast<int>(h_end - s.h_begin);
-  return s;
+// Walks the segments of a CTA's unit range with 32-bit counters: the range's first unit is
+// decomposed once (by one thread, for the whole CTA), then every role advances by carries, so
+// no warp divides 64-bit integers in its loop.  Unit u = ((b * nc + c) * MT + mt) * H + h.
+struct SegWalk {
+  int32_t b, c, mt, h, u, u_end;
+
+  __device__ __forceinline__ bool more() const { return u < u_end; }
+  __device__ __forceinline__ Segment seg(const ScParams& prm) const {
+    Segment s;
+    s.b = b;
+    s.c = c;
+    s.mt = mt;
+    s.h_begin = h;
+    s.g = h / prm.hpg;
+    s.nh = min((s.g + 1) * prm.hpg, h + (u_end - u)) - h;
+    return s;
+  }
+  __device__ __forceinline__ void advance(int nh, const ScParams& prm) {
+    u += nh;
+    h += nh;
+    if (h == prm.H) {
+      h = 0;
+      if (++mt == prm.MT) {
+        mt = 0;
+        if (++c == prm.nc) {
+          c = 0;
+          ++b;
+        }
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ SegWalk walk_from(int64_t u_begin, int64_t u_end, const ScParams& prm) {
+  SegWalk w;
+  const uint32_t u = static_cast<uint32_t>(u_begin);
+  const uint32_t bcm = u / uint32_t(prm.H), bc = bcm / uint32_t(prm.MT);
+  w.h = static_cast<int32_t>(u - bcm * uint32_t(prm.H));
+  w.mt = static_cast<int32_t>(bcm - bc * uint32_t(prm.MT));
+  w.c = static_cast<int32_t>(bc % uint32_t(prm.nc));
+  w.b = static_cast<int32_t>(bc / uint32_t(prm.nc));
+  w.u = static_cast<int32_t>(u_begin);
+  w.u_end = static_cast<int32_t>(u_end);
+  return w;
 }
 
 // One 32 x 32 block of P for this thread's row: P[row, j0 + e] = CB[row, j0 + e] * colf[e] *
@@ -229,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlot);
 
   if (threadIdx.x == 0) {
+    // this CTA's contiguous range of units, balanced by weight
+    *reinterpret_cast<SegWalk*>(smem + SM::kWalk) =
+        walk_from(unit_at_weight(prm.total_weight * blockIdx.x / gridDim.x, H, MT),
+                  unit_at_weight(prm.total_weight * (blockIdx.x + 1) / gridDim.x, H, MT), prm);
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_B);
     prefetch_tmap(&tm_C);
@@ -260,8 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that read them from global memory) wait for those in grid_dep_wait; the other roles only
   // see data through the producer's barriers
 
-  const int64_t u_begin = unit_at_weight(prm.total_weight * blockIdx.x / gridDim.x, H, MT);
-  const int64_t u_end = unit_at_weight(prm.total_weight * (blockIdx.x + 1) / gridDim.x, H, MT);
+  const SegWalk walk0 = *reinterpret_cast<const SegWalk*>(smem + SM::kWalk);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -294,16 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kernel before the previous one has completed): the first segment's C and B and the first
       // two heads' x are requested before waiting for the previous kernels
       int pre_x = 0;
-      if (u_begin < u_end) {
-        const Segment sg0 = segment_at(u_begin, u_end, prm);
+      if (walk0.more()) {
+        const Segment sg0 = walk0.seg(prm);
         load_cb(sg0);
         pend_cb = true;
         pre_x = sg0.nh < 2 ? sg0.nh : 2;
         for (int hi = 0; hi < pre_x; ++hi) load_x(sg0, sg0.h_begin + hi, uint32_t(hi));
       }
       grid_dep_wait();
-      for (int64_t u = u_begin; u < u_end; ++si) {
-        const Segment sg = segment_at(u, u_end, prm);
+      for (SegWalk w = walk0; w.more(); ++si) {
+        const Segment sg = w.seg(prm);
         const int i0 = sg.mt * 128, jrows = i0 + 128;
         // C and B of the new segment overwrite regions the previous segment's MMAs read
         if (si >= 1) (void)mbar_wait(bar(kSegFree), (si - 1) & 1, ctl);
@@ -339,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ph_xs[s] = use & 1;
           }
         }
-        u += sg.nh;
+        w.advance(sg.nh, prm);
       }
       // drain: every load issued must have landed before the CTA may exit
       if (pend_cb) (void)mbar_drain(bar(kCbFull), ph_cb, kWaitLimitNs);
@@ -355,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // queued MMAs have completed, which would serialise the groups.  The poller warp waits and
     // hands each "go" over through kBarIssue, at exactly the same points of the same schedule.
     uint32_t gi = 0;
-    for (int64_t u = u_begin; u < u_end;) {
-      const Segment sg = segment_at(u, u_end, prm);
+    for (SegWalk w = walk0; w.more();) {
+      const Segment sg = w.seg(prm);
       const int jrows = sg.mt * 128 + 128;
       const bool go_cb = issue_handoff(true);
       if (lane == 0) {
@@ -416,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) umma_commit(bar(kSegFree));
       __syncwarp();
-      u += sg.nh;
+      w.advance(sg.nh, prm);
     }
     if (lane == 0) {
       umma_commit(bar(kDrain));
@@ -427,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- poller for the MMA issuer
     // the issuer's waits, in its order; every wait is bounded, so every handoff is reached
     uint32_t gi = 0, si = 0, gpar = 0;  // gpar bit k: parity of P group k's uses so far
-    for (int64_t u = u_begin; u < u_end; ++si) {
-      const Segment sg = segment_at(u, u_end, prm);
+    for (SegWalk w = walk0; w.more(); ++si) {
+      const Segment sg = w.seg(prm);
       const int jrows = sg.mt * 128 + 128;
       const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
       const bool e = si == 0 || mbar_wait(bar(kCbEmpty), (si - 1) & 1, ctl);
@@ -445,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           gpar ^= 1u << k;
         }
       }
-      u += sg.nh;
+      w.advance(sg.nh, prm);
     }
   } else if (warp < 2 + kMaskWarps) {
     // ------------------------------------------------------------- mask: CB -> P in smem
@@ -455,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
     uint32_t gi = 0, si = 0;
     uint32_t gpar = 0, gused = 0;  // per P group: parity of its uses so far, used at least once
-    for (int64_t u = u_begin; u < u_end; ++si) {
-      const Segment sg = segment_at(u, u_end, prm);
+    for (SegWalk w = walk0; w.more(); ++si) {
+      const Segment sg = w.seg(prm);
       const int i0 = sg.mt * 128, jrows = i0 + 128, row = i0 + r;
       const int nblk = jrows / 32, maxblk = i0 / 32 + q;
       (void)mbar_wait(bar(kCbDone), si & 1, ctl);
@@ -532,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kCbEmpty));
-      u += sg.nh;
+      w.advance(sg.nh, prm);
     }
   } else if (warp < kPollWarp) {
     // ------------------------ epilogue: y = Y1 + 2^cs2_i Y2 -> staging -> TMA store of y
@@ -542,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool store_thread = warp == 2 + kMaskWarps && lane == 0;
     uint32_t gi = 0;
     grid_dep_wait();  // cs2 comes from the previous kernels
-    for (int64_t u = u_begin; u < u_end;) {
-      const Segment sg = segment_at(u, u_end, prm);
+    for (SegWalk w = walk0; w.more();) {
+      const Segment sg = w.seg(prm);
       const int i0 = sg.mt * 128, row = i0 + r;
       const bool tile_live = int64_t(sg.c) * Q + i0 < prm.L;
       for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
@@ -598,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
       }
-      u += sg.nh;
+      w.advance(sg.nh, prm);
     }
     if (store_thread) bulk_wait_read0();  // the stores have read the staging buffer
   }
