@@ -243,7 +243,7 @@ __device__ __forceinline__ void mask_block_exact(const uint32_t (&v)[32], const 
   }
 }
 
-template <int NB>
+template <int NB, bool ACC>  // ACC: add the y that earlier state slices stored
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_B,
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         1, 1, kMaskWarps, 1,                                  // cb_full cb_done cb_empty seg_free
         1, 1, 1, 1,                                           // hp_full[2] hp_empty[2]
         1, 1, 1 + kMaskWarps, 1 + kMaskWarps,                 // xs_full[2] xs_empty[2]
-        kMaskWarps, kMaskWarps, kMaskWarps, kMaskWarps,       // p_full[4]
+        kMaskWarps / 2, kMaskWarps / 2, kMaskWarps / 2, kMaskWarps / 2,  // p_full[4]: owners
         1, 1, 1, 1,                                           // p_empty[4]
         1, 1, kEpiWarps, kEpiWarps,                           // y_full[2] y_empty[2]
         1, 1};                                                // drain, spare
@@ -521,21 +521,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // group k holds 32-column blocks 2k and 2k+1; a quarter's four warps take its blocks
         // round-robin (warp sub owns block 2k + (sub & 1) of the groups k with k % 2 == sub / 2),
-        // so two groups are written at once.  The TMEM load of the block is issued before the
-        // wait for the group's P buffer; a warp owning nothing in a group arrives at once (the
-        // head-start barrier keeps every warp within one head of the others).
+        // so two groups are written at once, and only a group's eight owner warps (two per lane
+        // quarter) arrive on its barrier.  The TMEM load of the block is issued before the wait
+        // for the group's P buffer (the head-start barrier keeps every warp within one head of
+        // the others).
         const int ng = jrows / 64;
 #pragma unroll 1
-        for (int k = 0; k < ng; ++k) {
-          const bool owner = (k & 1) == (sub >> 1);
+        for (int k = sub >> 1; k < ng; k += 2) {
           const int blk = 2 * k + (sub & 1), j0 = 32 * blk;
-          const bool mine = live && owner && blk <= maxblk;
+          const bool mine = live && blk <= maxblk;
           uint32_t v[32];
           if (mine) {
             __syncwarp();
             tmem_ld32(trow + j0, v);
           }
-          const bool pfree = !owner || !((gused >> k) & 1u) ||
+          const bool pfree = !((gused >> k) & 1u) ||
                              mbar_wait(bar(kPEmpty0 + k), ((gpar >> k) & 1u) ^ 1u, ctl);
           if (mine) tmem_ld_wait();
           if (mine && pfree) {
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and, for a later state slice, the row of y the earlier slices wrote (a plain load: the
         // buffer is this kernel's output too)
         const uint4* prev_row =
-            prm.yacc && int64_t(sg.c) * Q + row < prm.L
+            ACC && int64_t(sg.c) * Q + row < prm.L
                 ? reinterpret_cast<const uint4*>(prm.yacc + ((int64_t(sg.b) * prm.L + int64_t(sg.c) * Q + row) * H + hh) * 64)
                 : nullptr;
         const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && !*abort_flag;
@@ -610,15 +610,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               const int cc = 2 * quarter + c2;
-              const uint4 pv = prev_row ? prev_row[cc] : make_uint4(0, 0, 0, 0);
+              // the earlier slices' y (ACC), widened and added before the one rounding
+              uint4 pv = make_uint4(0, 0, 0, 0);
+              if (ACC && prev_row) pv = prev_row[cc];
               const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
               uint32_t o[4];
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
                 const int k0 = 8 * c2 + 2 * e2;
-                o[e2] = pack_bf16x2(__uint_as_float(a[k0]) + e * __uint_as_float(q2[k0]) + bf16lo_to_f32(pw[e2]),
-                                    __uint_as_float(a[k0 + 1]) + e * __uint_as_float(q2[k0 + 1]) +
-                                        bf16hi_to_f32(pw[e2]));
+                float2 v2 = fma_f32x2(make_float2(e, e),
+                                      make_float2(__uint_as_float(q2[k0]), __uint_as_float(q2[k0 + 1])),
+                                      make_float2(__uint_as_float(a[k0]), __uint_as_float(a[k0 + 1])));
+                if (ACC) {
+                  v2.x += bf16lo_to_f32(pw[e2]);
+                  v2.y += bf16hi_to_f32(pw[e2]);
+                }
+                o[e2] = pack_bf16x2(v2.x, v2.y);
               }
               *reinterpret_cast<uint4*>(ys + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -652,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NB>
 cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cudaStream_t st) {
   using SM = ScSmem<NB>;
-  auto kern = chunk_scan_tc_kernel<NB>;
+  auto kern = prm.yacc ? chunk_scan_tc_kernel<NB, true> : chunk_scan_tc_kernel<NB, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, st, maps[0], maps[1], maps[2], maps[3],
