@@ -329,28 +329,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Packed float32 pair multiply (one instruction for two products).
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
-  uint64_t pa, pb, pr;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(pr) : "l"(pa), "l"(pb));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(pr));
-  return r;
-}
+// Packed float32 pair multiply (one instruction for two products), through the compiler's own
+// sm_100-family builtin so that it can place the pairs in register pairs itself.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // Packed float32 pair fused multiply-add a * b + c (one instruction for two).
-__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
-  uint64_t pa, pb, pc, pr;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(pr) : "l"(pa), "l"(pb), "l"(pc));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(pr));
-  return r;
-}
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // Two floats -> packed bf16x2 (round to nearest even); `lo` lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
