@@ -10,11 +10,21 @@
 // state dimension is the N axis, so both operands come straight from TMA in MN-major
 // 128-byte-swizzled form with no transposition.
 //
-// One CTA = (head pair, n-tile, chunk, batch), 128 threads, no warp specialisation:
-//   thread 0 issues TMA loads (2-stage ring over 64-token k-blocks) and the MMAs;
-//   all threads scale the x tile in shared memory by the per-token decay weight
-//   (one scale per 128-byte row, so the swizzle is irrelevant), then drain the f32
-//   accumulator from tensor memory and stage it, rounded to bf16, for TMA stores of S.
+// Persistent CTAs (one per SM) walk the work items (head pair, n-tile, chunk, batch) with a
+// stride of the grid size, so the CTAs running at one time share a chunk's B through L2.  Warp
+// roles, synchronised through mbarriers so that one item's epilogue overlaps the next items'
+// loads and MMAs:
+//   warp 0      TMA producer: per 64-token k-block one box of both heads' x and one of B's NT
+//               columns into a ring of kStages stages that runs on across items; per item the
+//               two heads' cs2 / dt rows (bulk copies) into one of two weight windows;
+//   warp 1      tcgen05.mma issuer: per k-block 4 MMAs (M = 2 x P = 128, N = NT, K = 16) into
+//               one of two TMEM accumulators (the item's parity);
+//   warps 2-5   the decay weights w_t = 2^{cs2_last - cs2_t} dt_t of each item, then x~ = w x
+//               in place in every stage (one weight per 128-byte row, so the swizzle does not
+//               matter);
+//   warps 6-9   epilogue: accumulator -> bf16 -> swizzled staging -> TMA store of S.
+// Every wait is bounded; after an expiry the roles keep their loop counts but skip their work,
+// then drain their own copies and MMAs and release TMEM.
 // Requirements (checked by chunk_state_tc_ok): bf16 I/O, P = 64, Q in {128, 256},
 // N in {64, 128, 256, 512} (512 runs as two 256-wide n-tiles).
 #include "ptx.cuh"
@@ -23,11 +33,15 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 10;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kScaleWarp0 = 2, kEpiWarp0 = 6;
 constexpr uint32_t kBox = 8192;  // one TMA box: 64 rows x 128 bytes
+constexpr uint32_t kBarScale = 1, kBarEpi = 2;  // named barriers of the scale and epilogue groups
 
 struct CsParams {
   int32_t L, H, nc, Q, N, hpg, pairs_per_group, n_tiles;
+  int64_t items;
   const float* cs2;
   const float* dtT;
   uint32_t* status;
@@ -36,6 +50,310 @@ struct CsParams {
 
 template <int NT>
 struct CsSmem {
+  static constexpr uint32_t kX = 2 * kBox;                  // x: two heads x (64 tokens x 64 p)
+  static constexpr uint32_t kB = (NT / 64) * kBox;          // B: NT/64 boxes of (64 tokens x 64 n)
+  static constexpr uint32_t kStage = kX + kB;
+  static constexpr int kStages = NT == 256 ? 3 : (NT == 128 ? 5 : 6);
+  static constexpr uint32_t kOut = kStages * kStage;        // S staging: NT/64 x 2 boxes
+  static constexpr uint32_t kWin = kOut + 2 * (NT / 64) * kBox;  // 2 windows: cs2, dt rows of 2 heads
+  static constexpr uint32_t kWinBytes = 4 * 256 * 4;
+  static constexpr uint32_t kW = kWin + 2 * kWinBytes;      // 2 x float w[2][256]
+  static constexpr uint32_t kBars = kW + 2 * 2048;
+  static constexpr int kNumBars = 3 * kStages + 9;
+  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kUsed = kAbort + 4;
+  static constexpr uint32_t kAlloc = kUsed + 1024;          // slack for 1024-byte alignment
+  static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
+  // mbarrier indices
+  static constexpr int kFull = 0, kScaled = kStages, kEmpty = 2 * kStages, kWinFull = 3 * kStages,
+                       kWinEmpty = kWinFull + 2, kAccFull = kWinEmpty + 2, kAccEmpty = kAccFull + 2,
+                       kDrain = kAccEmpty + 2;
+};
+
+// One work item: (head pair, n-tile) fastest, then chunk, then batch.
+struct Item {
+  int b, c, g, h0, nh, nt;
+};
+__device__ __forceinline__ Item item_at(int64_t i, const CsParams& prm) {
+  Item it;
+  const int64_t per_c = int64_t(prm.H / prm.hpg) * prm.pairs_per_group * prm.n_tiles;
+  const int64_t bc = i / per_c;
+  const int rem = static_cast<int>(i - bc * per_c);
+  it.nt = rem % prm.n_tiles;
+  const int pair = rem / prm.n_tiles;
+  it.g = pair / prm.pairs_per_group;
+  it.h0 = it.g * prm.hpg + 2 * (pair % prm.pairs_per_group);
+  it.nh = min(2, (it.g + 1) * prm.hpg - it.h0);  // 1 when the group has an odd head count
+  it.c = static_cast<int>(bc % prm.nc);
+  it.b = static_cast<int>(bc / prm.nc);
+  return it;
+}
+
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
+  return pack_bf16x2(bf16lo_to_f32(v) * w, bf16hi_to_f32(v) * w);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_B,
+                          const __grid_constant__ CUtensorMap tm_S, const CsParams prm) {
+  using SM = CsSmem<NT>;
+  constexpr int S = SM::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Q = prm.Q, kblocks = Q / 64;
+  auto bar = [&](int i) { return sb + SM::kBars + 8u * i; };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM::kAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlot);
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_B);
+    prefetch_tmap(&tm_S);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(bar(SM::kFull + i), 1);
+      mbar_init(bar(SM::kScaled + i), 4);
+      mbar_init(bar(SM::kEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(SM::kWinFull + i), 1);
+      mbar_init(bar(SM::kWinEmpty + i), 4);
+      mbar_init(bar(SM::kAccFull + i), 1);
+      mbar_init(bar(SM::kAccEmpty + i), 4);
+    }
+    mbar_init(bar(SM::kDrain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), 2 * NT);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
+  const int64_t i0 = blockIdx.x, istep = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool pend_full[S], pend_win[2] = {false, false};
+      uint32_t ph_full[S], ph_win[2] = {0, 0};
+      for (int i = 0; i < S; ++i) pend_full[i] = false, ph_full[i] = 0;
+      uint32_t gk = 0, it_local = 0;
+      // x and B are inputs of the step: the first item's k-blocks are requested before waiting
+      // for the previous kernel (cs2 / dtT come from it)
+      const int pre = i0 < prm.items ? (kblocks < S ? kblocks : S) : 0;
+      auto load_kb = [&](const Item& it, int kb, uint32_t k) {
+        const int s = static_cast<int>(k % S);
+        const uint32_t st = sb + s * SM::kStage, full = bar(SM::kFull + s);
+        const int t0 = it.c * Q + kb * 64;
+        mbar_arrive_expect_tx(full, SM::kStage);
+        tma_load_4d(st, &tm_x, full, 0, t0, it.h0, it.b);
+        tma_load_4d(st + SM::kX, &tm_B, full, 0, t0, (it.g * prm.N + it.nt * NT) / 64, it.b);
+        pend_full[s] = true;
+        ph_full[s] = (k / S) & 1;
+      };
+      if (pre > 0) {
+        const Item it = item_at(i0, prm);
+        for (int kb = 0; kb < pre; ++kb) load_kb(it, kb, uint32_t(kb));
+      }
+      grid_dep_wait();
+      for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
+        const Item it = item_at(i, prm);
+        const uint32_t ws = it_local & 1;
+        if (it_local >= 2) (void)mbar_wait(bar(SM::kWinEmpty + ws), ((it_local >> 1) - 1) & 1, ctl);
+        if (!*abort_flag) {
+          const uint32_t win = sb + SM::kWin + ws * SM::kWinBytes, wf = bar(SM::kWinFull + ws);
+          mbar_arrive_expect_tx(wf, it.nh * 2 * Q * 4);
+          for (int k = 0; k < it.nh; ++k) {
+            const int64_t row = ((int64_t(it.b) * prm.H + it.h0 + k) * prm.nc + it.c) * Q;
+            bulk_load(win + k * 1024, prm.cs2 + row, Q * 4, wf);
+            bulk_load(win + 2048 + k * 1024, prm.dtT + row, Q * 4, wf);
+          }
+          pend_win[ws] = true;
+          ph_win[ws] = (it_local >> 1) & 1;
+        }
+        for (int kb = 0; kb < kblocks; ++kb, ++gk) {
+          if (it_local == 0 && kb < pre) continue;  // requested before the wait
+          const int s = static_cast<int>(gk % S);
+          if (gk >= uint32_t(S)) (void)mbar_wait(bar(SM::kEmpty + s), ((gk / S) - 1) & 1, ctl);
+          if (!*abort_flag) load_kb(it, kb, gk);
+        }
+      }
+      // drain: every load issued must have landed before the CTA may exit
+      for (int s = 0; s < S; ++s)
+        if (pend_full[s]) (void)mbar_drain(bar(SM::kFull + s), ph_full[s], kWaitLimitNs);
+      for (int w = 0; w < 2; ++w)
+        if (pend_win[w]) (void)mbar_drain(bar(SM::kWinFull + w), ph_win[w], kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, NT, 1, 1);
+    uint32_t gk = 0, it_local = 0;
+    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
+      const uint32_t a = it_local & 1;
+      if (it_local >= 2) (void)mbar_wait(bar(SM::kAccEmpty + a), ((it_local >> 1) - 1) & 1, ctl);
+      for (int kb = 0; kb < kblocks; ++kb, ++gk) {
+        const int s = static_cast<int>(gk % S);
+        const bool ok = mbar_wait(bar(SM::kScaled + s), (gk / S) & 1, ctl) && !*abort_flag;
+        if (lane == 0) {
+          if (ok) {
+            tc_fence_after();
+            const uint32_t xa = sb + s * SM::kStage, ba = xa + SM::kX;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_f16(tmem + a * NT, sdesc_sw128(xa + k * 2048, kBox, 1024),
+                       sdesc_sw128(ba + k * 2048, kBox, 1024), kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(bar(SM::kEmpty + s));
+        }
+        __syncwarp();
+      }
+      if (lane == 0) umma_commit(bar(SM::kAccFull + a));
+      __syncwarp();
+    }
+    if (lane == 0) {
+      umma_commit(bar(SM::kDrain));
+      (void)mbar_drain(bar(SM::kDrain), 0, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------- decay weights, x~ = w x in place
+    const int ts = threadIdx.x - 32 * kScaleWarp0;  // 0..127
+    uint32_t gk = 0, it_local = 0;
+    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
+      const Item it = item_at(i, prm);
+      const uint32_t ws = it_local & 1;
+      const bool have = mbar_wait(bar(SM::kWinFull + ws), (it_local >> 1) & 1, ctl);
+      const float* win = reinterpret_cast<const float*>(smem + SM::kWin + ws * SM::kWinBytes);
+      float* wsm = reinterpret_cast<float*>(smem + SM::kW + ws * 2048);
+      for (int e = ts; e < 2 * Q; e += 128) {
+        const int k = e / Q, t = e % Q;
+        // w[k][t] = 2^(cs2_last - cs2_t) dt_t; zero for a missing second head
+        wsm[k * 256 + t] = have && k < it.nh ? ex2(win[k * 256 + Q - 1] - win[k * 256 + t]) * win[512 + k * 256 + t] : 0.f;
+      }
+      named_bar_sync(kBarScale, 128);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SM::kWinEmpty + ws));
+      for (int kb = 0; kb < kblocks; ++kb, ++gk) {
+        const int s = static_cast<int>(gk % S);
+        const bool ok = mbar_wait(bar(SM::kFull + s), (gk / S) & 1, ctl) && !*abort_flag;
+        if (ok) {
+          // 1024 16-byte chunks (two boxes x 64 rows x 8), 8 per thread
+          uint8_t* xs = smem + s * SM::kStage;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int q = ts + 128 * j;
+            const int k = q >> 9, r = (q >> 3) & 63;
+            const float w = wsm[k * 256 + kb * 64 + r];
+            uint4* pch = reinterpret_cast<uint4*>(xs + q * 16);
+            uint4 v = *pch;
+            v.x = scale_bf16x2(v.x, w);
+            v.y = scale_bf16x2(v.y, w);
+            v.z = scale_bf16x2(v.z, w);
+            v.w = scale_bf16x2(v.w, w);
+            *pch = v;
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(SM::kScaled + s));
+      }
+    }
+  } else {
+    // --------------------------------- epilogue: accumulator -> bf16 -> TMA store of S
+    const int q4 = warp & 3, r = 32 * q4 + lane;  // TMEM lane quarter; accumulator row = (head, p)
+    const int k = r >> 6, pr = r & 63;
+    const bool store_thread = warp == kEpiWarp0 && lane == 0;
+    uint32_t it_local = 0;
+    grid_dep_wait();  // S may still be read by the kernels before the previous one
+    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
+      const Item it = item_at(i, prm);
+      const uint32_t a = it_local & 1;
+      const bool ok = mbar_wait(bar(SM::kAccFull + a), (it_local >> 1) & 1, ctl) && !*abort_flag;
+      tc_fence_after();
+      if (store_thread) bulk_wait_read0();  // the staging buffer is free again
+      named_bar_sync(kBarEpi, 128);
+      if (ok) {
+#pragma unroll 1
+        for (int q = 0; q < NT / 32; ++q) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tmem + a * NT + (uint32_t(32 * q4) << 16) + q * 32, v);
+          tmem_ld_wait();
+          uint8_t* box = smem + SM::kOut + ((q >> 1) * 2 + k) * kBox;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int cc = (q & 1) * 4 + c4;
+            *reinterpret_cast<uint4*>(box + pr * 128 + ((cc ^ (pr & 7)) << 4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SM::kAccEmpty + a));
+      fence_proxy_async_smem();
+      named_bar_sync(kBarEpi, 128);
+      if (store_thread && ok) {
+        for (int j = 0; j < NT / 64; ++j)
+          for (int kk = 0; kk < it.nh; ++kk)
+            tma_store_2d(&tm_S, sb + SM::kOut + (j * 2 + kk) * kBox, it.nt * NT + j * 64,
+                         ((it.b * prm.nc + it.c) * prm.H + it.h0 + kk) * 64);
+        bulk_commit();
+      }
+    }
+    if (store_thread) bulk_wait_read0();  // the stores have read the staging buffer
+  }
+
+  grid_dep_launch();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * NT);
+  }
+}
+
+template <int NT>
+cudaError_t launch_nt(const CUtensorMap& tx, const CUtensorMap& tb, const CUtensorMap& ts,
+                      const CsParams& prm, cudaStream_t st) {
+  using SM = CsSmem<NT>;
+  auto kern = chunk_state_tc_kernel<NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  if (e != cudaSuccess) return e;
+  int sms = num_sms_current_device();
+  if (sms <= 0) sms = 1;
+  const int64_t grid = prm.items < sms ? prm.items : sms;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), SM::kAlloc, st, tx, tb, ts, prm);
+}
+
+// ---- one CTA per work item: the first design, kept for problems with few items per SM ----
+//
+// One CTA = (head pair, n-tile, chunk, batch), 128 threads, no warp specialisation: thread 0
+// issues TMA loads (2-stage ring over 64-token k-blocks) and the MMAs; all threads scale the x
+// tile in shared memory by the decay weight, then drain the f32 accumulator from tensor memory
+// and stage it, rounded to bf16, for TMA stores of S.  Several CTAs share an SM, so their
+// load, MMA and store phases overlap one another; with a few items per SM that beats the
+// persistent kernel's single pipeline (130M layer 15.5 against 18.4 us), with many it loses
+// (2.7B layer 62 against 58 us, 256K tokens 366 against 316 us).
+constexpr int kItemThreads = 128;
+
+template <int NT>
+struct ItemSmem {
   static constexpr uint32_t kX = 2 * kBox;            // x: two heads x (64 tokens x 64 p)
   static constexpr uint32_t kB = (NT / 64) * kBox;    // B: NT/64 boxes of (64 tokens x 64 n)
   static constexpr uint32_t kStage = kX + kB;
@@ -49,16 +367,12 @@ struct CsSmem {
   static_assert((NT / 64) * 2 * kBox <= kTiles, "epilogue staging must fit in the ring");
 };
 
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
-  return pack_bf16x2(bf16lo_to_f32(v) * w, bf16hi_to_f32(v) * w);
-}
-
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
-    chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(kItemThreads, 1)
+    chunk_state_item_kernel(const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_B,
                           const __grid_constant__ CUtensorMap tm_S, const CsParams prm) {
-  using SM = CsSmem<NT>;
+  using SM = ItemSmem<NT>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -120,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dep_wait();  // cs2 / dtT come from the previous kernel; S may still be read by older ones
   // decay weights of the (up to) two heads: w[k][t] = 2^(cs2_last - cs2_t) * dt_t
-  for (int e = tid; e < 2 * Q; e += kThreads) {
+  for (int e = tid; e < 2 * Q; e += kItemThreads) {
     const int k = e / Q, t = e % Q;
     float w = 0.f;
     if (k < nh) {
@@ -146,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* xs = smem + s * SM::kStage;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int q = tid + kThreads * i;
+        const int q = tid + kItemThreads * i;
         const int k = q >> 9, r = (q >> 3) & 63;
         const float w = wsm[k * 256 + kb * 64 + r];
         uint4* p = reinterpret_cast<uint4*>(xs + q * 16);
@@ -233,18 +547,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NT>
-cudaError_t launch_nt(const Problem& p, const CUtensorMap& tx, const CUtensorMap& tb,
+cudaError_t launch_item_nt(const Problem& p, const CUtensorMap& tx, const CUtensorMap& tb,
                       const CUtensorMap& ts, const CsParams& prm, cudaStream_t st) {
-  using SM = CsSmem<NT>;
-  auto kern = chunk_state_tc_kernel<NT>;
+  using SM = ItemSmem<NT>;
+  auto kern = chunk_state_item_kernel<NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.G * prm.pairs_per_group * prm.n_tiles),
                   static_cast<unsigned>(p.nc), static_cast<unsigned>(p.b));
-  return launch_pdl(kern, grid, dim3(kThreads), SM::kAlloc, st, tx, tb, ts, prm);
+  return launch_pdl(kern, grid, dim3(kItemThreads), SM::kAlloc, st, tx, tb, ts, prm);
 }
 
 }  // namespace
+
+// Items per SM from which the persistent kernel runs (measured: 2.5 and 6.7 per SM favour one
+// CTA per item, 13.5 and more the persistent kernel).
+constexpr int64_t kPersistentItemsPerSm = 12;
 
 bool chunk_state_tc_ok(const Problem& p) {
   return p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) &&
@@ -294,14 +612,26 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.pairs_per_group = static_cast<int32_t>((p.hpg + 1) / 2);
   prm.n_tiles = static_cast<int32_t>(p.N / NT);
+  prm.items = p.b * p.nc * p.G * prm.pairs_per_group * prm.n_tiles;
   prm.cs2 = cs2;
   prm.dtT = dtT;
   prm.status = status;
   prm.wait_ns = kWaitLimitNs;
-  switch (NT) {
-    case 64: return launch_nt<64>(p, tx, tb, ts, prm, st);
-    case 128: return launch_nt<128>(p, tx, tb, ts, prm, st);
-    case 256: return launch_nt<256>(p, tx, tb, ts, prm, st);
+  // the persistent kernel once every SM gets a dozen items or more, one CTA per item below that
+  int sms = num_sms_current_device();
+  if (sms <= 0) sms = 1;
+  if (prm.items >= kPersistentItemsPerSm * int64_t(sms)) {
+    switch (NT) {
+      case 64: return launch_nt<64>(tx, tb, ts, prm, st);
+      case 128: return launch_nt<128>(tx, tb, ts, prm, st);
+      case 256: return launch_nt<256>(tx, tb, ts, prm, st);
+    }
+  } else {
+    switch (NT) {
+      case 64: return launch_item_nt<64>(p, tx, tb, ts, prm, st);
+      case 128: return launch_item_nt<128>(p, tx, tb, ts, prm, st);
+      case 256: return launch_item_nt<256>(p, tx, tb, ts, prm, st);
+    }
   }
   return cudaErrorInvalidValue;
 }

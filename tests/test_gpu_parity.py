@@ -120,6 +120,18 @@ def test_edge_shapes(shape, dtype):
     check_against_oracle(inp)
 
 
+@pytest.mark.parametrize("shape", [
+    # odd heads per group (a pair with one head), two groups, ragged end
+    dict(batch=1, seqlen=118000, nheads=6, headdim=64, dstate=128, ngroups=2, chunk=256),
+    dict(batch=1, seqlen=117760, nheads=8, headdim=64, dstate=64, chunk=256),
+], ids=["g2_odd_heads", "n64"])
+def test_persistent_chunk_state_shapes(shape):
+    # enough (head pair, n-tile, chunk) items for chunk_state's persistent kernel (a dozen or
+    # more per SM); every head compared with the oracle over the whole sequence
+    inp = synth.make_inputs(io_dtype="bf16", init=True, seed=41, **shape)
+    check_against_oracle(inp)
+
+
 def test_cumsum_32_head_tiles():
     # H a multiple of 32 and enough chunks: chunk_cumsum stages 32 heads per CTA (whole
     # 128-byte rows of dt); ragged last chunk
