@@ -622,10 +622,10 @@ def run_ours(args):
 
 
 def scan_launches(shape, plan):
-    """Launches of the chunk_scan step: the tensor-core kernel runs once per 128 state columns
-    when the state is larger than 128."""
-    n = shape["dstate"]
-    return n // 128 if (plan & 2) and n > 128 else 1
+    """Launches of the chunk_scan step: with states above 128 columns the tensor-core path runs
+    the readout kernel (the term through the chunk-start state) before chunk_scan."""
+    n, q = shape["dstate"], shape["chunk"]
+    return 2 if (plan & 2) and n > 128 and n % 64 == 0 and n >= q else 1
 
 
 def run_bwd(args, torch, dist, ssd, synth, ws, rank, local, dev):

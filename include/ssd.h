@@ -88,7 +88,11 @@ typedef struct {
  *         when io_dtype is SSD_BF16, float32 when SSD_F32
  *   hprev (b, nc, H, P, N): state entering each chunk; bfloat16 when
  *         io_dtype is SSD_BF16, float32 when SSD_F32
- *   status uint32 at offset 0: 0, or an ssd_status recorded by a kernel      */
+ *   status uint32 at offset 0: 0, or an ssd_status recorded by a kernel
+ * With bf16 I/O, headdim 64 and dstate above 128 (a multiple of 64, not
+ * below chunk), chunk_scan first computes the term through the chunk-start
+ * state, 2^{cs2_i} C_i . hprev, as a bf16 (b, L, H, P) tensor in the S
+ * region (S is dead by then); S then holds that tensor on return.          */
 typedef struct {
   size_t status, cs2, dtT, S, hprev, total;
   int64_t nchunks;

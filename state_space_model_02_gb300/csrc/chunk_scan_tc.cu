@@ -40,9 +40,12 @@
 // Every wait is bounded; after an expiry all roles keep their loop trip counts (so named
 // barriers stay matched) but skip their work, then drain and release TMEM.
 // Requirements (chunk_scan_tc_ok): bf16 I/O, P = 64, Q in {128, 256}, N in {64, 128}, or N a
-// multiple of 128 up to 512: y is linear in the state columns (CB and Y2 are sums over them, the
-// mask and the decays act element-wise), so larger states run one launch per 128-column slice,
-// D on the first only; each later slice's epilogue adds the bf16 y its predecessors stored.
+// multiple of 64 above 128 with N >= Q (WIDE).  A WIDE launch cannot keep the m-tile's C rows
+// (128 x N) beside its other operands in shared memory: CB is built by a K loop over the state
+// in 64-column steps (C and B tiles through two slots), and the term through hprev, Z =
+// 2^{cs2_i} C_m hprev^T, comes from the readout kernel (chunk_readout_tc.cu), which runs first
+// and leaves Z in bf16; the producer loads each head's Z rows into the hprev slot and the
+// epilogue adds them (y = Y1 + Z), so no per-head C.hprev^T runs here.
 #include "ptx.cuh"
 #include "ssd_internal.h"
 
@@ -81,9 +84,7 @@ __device__ __forceinline__ bool issue_handoff(bool ok) {
 
 struct ScParams {
   int32_t L, H, nc, Q, N, hpg, MT;
-  int32_t col0;  // first state column of this launch's slice (C and B are N columns per group)
   int64_t units, total_weight;
-  const uint16_t* yacc;  // y of the previous slices, added to this one's (null: first slice)
   const float* cs2;
   const float* dtT;
   const float* D;
@@ -106,7 +107,7 @@ struct ScSmem {
   static constexpr uint32_t kY = kXs0 + 2 * kXsBytes;        // 16 KB: y staging (128 rows x 128 B)
   static constexpr uint32_t kColf = kY + kBox128;            // 2 x 1 KB: per-head column factors
   static constexpr uint32_t kBars = kColf + 2048;
-  static constexpr int kNumBars = 26;
+  static constexpr int kNumBars = 30;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kWalk = kAbort + 4;              // SegWalk of the CTA's first unit
@@ -120,7 +121,8 @@ struct ScSmem {
 enum : int {
   kCbFull = 0, kCbDone, kCbEmpty, kSegFree, kHpFull0, kHpFull1, kHpEmpty0, kHpEmpty1,
   kXsFull0, kXsFull1, kXsEmpty0, kXsEmpty1, kPFull0, kPEmpty0 = kPFull0 + 4,
-  kYFull0 = kPEmpty0 + 4, kYFull1, kYEmpty0, kYEmpty1, kDrain
+  kYFull0 = kPEmpty0 + 4, kYFull1, kYEmpty0, kYEmpty1, kDrain,
+  kCbK0, kCbK1, kCbKEmpty0, kCbKEmpty1  // WIDE: the two (C, B) K-step slots of the CB phase
 };
 
 // Work weights of the two 128-row m-tiles of a 256-token chunk (the second one's causal
@@ -243,12 +245,12 @@ __device__ __forceinline__ void mask_block_exact(const uint32_t (&v)[32], const 
   }
 }
 
-template <int NB, bool ACC>  // ACC: add the y that earlier state slices stored
+template <int NB, bool WIDE>  // WIDE: state above 128 columns (CB by a K loop, Z from the readout)
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_B,
                          const __grid_constant__ CUtensorMap tm_C,
-                         const __grid_constant__ CUtensorMap tm_h,
+                         const __grid_constant__ CUtensorMap tm_h,  // hprev, or Z when WIDE
                          const __grid_constant__ CUtensorMap tm_y, const ScParams prm) {
   using SM = ScSmem<NB>;
   extern __shared__ uint8_t smem_raw[];
@@ -273,12 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_y);
     const uint32_t counts[SM::kNumBars] = {
         1, 1, kMaskWarps, 1,                                  // cb_full cb_done cb_empty seg_free
-        1, 1, 1, 1,                                           // hp_full[2] hp_empty[2]
+        1, 1, WIDE ? kEpiWarps : 1, WIDE ? kEpiWarps : 1,     // hp_full[2] hp_empty[2]
         1, 1, 1 + kMaskWarps, 1 + kMaskWarps,                 // xs_full[2] xs_empty[2]
         kMaskWarps / 2, kMaskWarps / 2, kMaskWarps / 2, kMaskWarps / 2,  // p_full[4]: owners
         1, 1, 1, 1,                                           // p_empty[4]
         1, 1, kEpiWarps, kEpiWarps,                           // y_full[2] y_empty[2]
-        1, 1};                                                // drain, spare
+        1, 1,                                                 // drain, spare
+        1, 1, 1, 1};                                          // cbk_full[2] cbk_empty[2]
     for (int i = 0; i < SM::kNumBars; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -302,19 +305,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t gi = 0, si = 0;
+      uint32_t gi = 0, si = 0, cbk = 0;
       bool pend_cb = false, pend_hp[2] = {false, false}, pend_xs[2] = {false, false};
-      uint32_t ph_cb = 0, ph_hp[2] = {0, 0}, ph_xs[2] = {0, 0};
+      bool pend_cbk[2] = {false, false};
+      uint32_t ph_cb = 0, ph_hp[2] = {0, 0}, ph_xs[2] = {0, 0}, ph_cbk[2] = {0, 0};
       auto load_cb = [&](const Segment& sg) {
         const int i0 = sg.mt * 128, jrows = i0 + 128;
         mbar_arrive_expect_tx(bar(kCbFull), NB * kBox128 + NB * jrows * 128);
         for (int nb = 0; nb < NB; ++nb)
-          tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + prm.col0 + nb * 64,
+          tma_load_3d(sb + SM::kC + nb * kBox128, &tm_C, bar(kCbFull), sg.g * N + nb * 64,
                       sg.c * Q + i0, sg.b);
         for (int nb = 0; nb < NB; ++nb)
           for (int jb = 0; jb < jrows / 128; ++jb)
             tma_load_3d(sb + SM::kP + nb * jrows * 128 + jb * kBox128, &tm_B, bar(kCbFull),
-                        sg.g * N + prm.col0 + nb * 64, sg.c * Q + jb * 128, sg.b);
+                        sg.g * N + nb * 64, sg.c * Q + jb * 128, sg.b);
+      };
+      // WIDE: the segment's CB operands as N / 64 K steps of 64 state columns, each C tile
+      // (128 rows) and B tile (jrows rows) into slot cbk % 2 (C region, P region halves)
+      auto load_cb_wide = [&](const Segment& sg) {
+        const int i0 = sg.mt * 128, jrows = i0 + 128;
+        for (int k = 0; k < N / 64; ++k, ++cbk) {
+          const uint32_t slot = cbk & 1;
+          if (cbk >= 2) (void)mbar_wait(bar(kCbKEmpty0 + slot), ((cbk >> 1) - 1) & 1, ctl);
+          if (*abort_flag) continue;
+          const uint32_t fb = bar(kCbK0 + slot);
+          mbar_arrive_expect_tx(fb, kBox128 + jrows * 128);
+          tma_load_3d(sb + SM::kC + slot * kBox128, &tm_C, fb, sg.g * N + 64 * k, sg.c * Q + i0, sg.b);
+          for (int jb = 0; jb < jrows / 128; ++jb)
+            tma_load_3d(sb + SM::kP + slot * 32768 + jb * kBox128, &tm_B, fb, sg.g * N + 64 * k,
+                        sg.c * Q + jb * 128, sg.b);
+          pend_cbk[slot] = true;
+          ph_cbk[slot] = (cbk >> 1) & 1;
+        }
       };
       // x slot s of a head: its x box(es) now, its cs2 / dt rows (from the previous kernel) later;
       // the slot's barrier expects all three from the start
@@ -332,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pre_x = 0;
       if (walk0.more()) {
         const Segment sg0 = walk0.seg(prm);
-        load_cb(sg0);
-        pend_cb = true;
+        if (!WIDE) {
+          load_cb(sg0);
+          pend_cb = true;
+        }
         pre_x = sg0.nh < 2 ? sg0.nh : 2;
         for (int hi = 0; hi < pre_x; ++hi) load_x(sg0, sg0.h_begin + hi, uint32_t(hi));
       }
@@ -343,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i0 = sg.mt * 128, jrows = i0 + 128;
         // C and B of the new segment overwrite regions the previous segment's MMAs read
         if (si >= 1) (void)mbar_wait(bar(kSegFree), (si - 1) & 1, ctl);
-        if (si >= 1 && !*abort_flag) {
+        if (WIDE) {
+          load_cb_wide(sg);
+        } else if (si >= 1 && !*abort_flag) {
           load_cb(sg);
           pend_cb = true;
           ph_cb = si & 1;
@@ -356,9 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!*abort_flag) {
             const uint32_t hb = bar(kHpFull0 + s);
             mbar_arrive_expect_tx(hb, SM::kHpBytes);
-            // one 3-D box brings both 64-column halves of the head's state (NB 8 KB tiles)
-            tma_load_3d(sb + SM::kHp0 + s * SM::kHpBytes, &tm_h, hb, 0,
-                        ((sg.b * prm.nc + sg.c) * H + hh) * 64, 0);
+            if (WIDE)  // the head's Z rows of the m-tile (128 rows x 64 p)
+              tma_load_3d(sb + SM::kHp0 + s * SM::kHpBytes, &tm_h, hb, hh * 64, sg.c * Q + i0, sg.b);
+            else  // one 3-D box brings both 64-column halves of the head's state (NB 8 KB tiles)
+              tma_load_3d(sb + SM::kHp0 + s * SM::kHpBytes, &tm_h, hb, 0,
+                          ((sg.b * prm.nc + sg.c) * H + hh) * 64, 0);
             pend_hp[s] = true;
             ph_hp[s] = use & 1;
           }
@@ -380,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every load issued must have landed before the CTA may exit
       if (pend_cb) (void)mbar_drain(bar(kCbFull), ph_cb, kWaitLimitNs);
       for (int s = 0; s < 2; ++s) {
+        if (pend_cbk[s]) (void)mbar_drain(bar(kCbK0 + s), ph_cbk[s], kWaitLimitNs);
         if (pend_hp[s]) (void)mbar_drain(bar(kHpFull0 + s), ph_hp[s], kWaitLimitNs);
         if (pend_xs[s]) (void)mbar_drain(bar(kXsFull0 + s), ph_xs[s], kWaitLimitNs);
       }
@@ -390,32 +419,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reads the abort flag itself: a shared-memory access by the issuing thread stalls until its
     // queued MMAs have completed, which would serialise the groups.  The poller warp waits and
     // hands each "go" over through kBarIssue, at exactly the same points of the same schedule.
-    uint32_t gi = 0;
+    uint32_t gi = 0, cbk = 0;
     for (SegWalk w = walk0; w.more();) {
       const Segment sg = w.seg(prm);
       const int jrows = sg.mt * 128 + 128;
-      const bool go_cb = issue_handoff(true);
-      if (lane == 0) {
-        if (go_cb) {
-          tc_fence_after();
-          const uint32_t idesc = idesc_bf16_f32(128, jrows, 0, 0);
-          for (int nb = 0; nb < NB; ++nb)
+      const uint32_t idesc_cb = idesc_bf16_f32(128, jrows, 0, 0);
+      if (WIDE) {
+        // CB = sum over the K steps of C_k B_k^T
+        for (int k = 0; k < N / 64; ++k, ++cbk) {
+          const uint32_t slot = cbk & 1;
+          const bool go = issue_handoff(true);
+          if (lane == 0) {
+            if (go) {
+              tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_f16(tmem, sdesc_sw128(sb + SM::kC + nb * kBox128 + k * 32, 16, 1024),
-                       sdesc_sw128(sb + SM::kP + nb * jrows * 128 + k * 32, 16, 1024), idesc,
-                       (nb | k) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16(tmem, sdesc_sw128(sb + SM::kC + slot * kBox128 + kk * 32, 16, 1024),
+                         sdesc_sw128(sb + SM::kP + slot * 32768 + kk * 32, 16, 1024), idesc_cb,
+                         (k | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(bar(kCbKEmpty0 + slot));
+          }
+          __syncwarp();
         }
-        umma_commit(bar(kCbDone));
+        if (lane == 0) umma_commit(bar(kCbDone));
+        __syncwarp();
+      } else {
+        const bool go_cb = issue_handoff(true);
+        if (lane == 0) {
+          if (go_cb) {
+            tc_fence_after();
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_f16(tmem, sdesc_sw128(sb + SM::kC + nb * kBox128 + k * 32, 16, 1024),
+                         sdesc_sw128(sb + SM::kP + nb * jrows * 128 + k * 32, 16, 1024), idesc_cb,
+                         (nb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(bar(kCbDone));
+        }
+        __syncwarp();
       }
-      __syncwarp();
       for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
         const uint32_t s = gi & 1;
         const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
         const uint32_t hp = sb + SM::kHp0 + s * SM::kHpBytes;
         const uint32_t ycol = 256 + 128 * s;
-        const bool go_y2 = issue_handoff(true);
-        if (lane == 0) {
+        const bool go_y2 = WIDE || issue_handoff(true);  // WIDE: Z comes from the readout
+        if (!WIDE && lane == 0) {
           if (go_y2) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
@@ -462,18 +513,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kPollWarp) {
     // ----------------------------------------------------- poller for the MMA issuer
     // the issuer's waits, in its order; every wait is bounded, so every handoff is reached
-    uint32_t gi = 0, si = 0, gpar = 0;  // gpar bit k: parity of P group k's uses so far
+    uint32_t gi = 0, si = 0, gpar = 0, cbk = 0;  // gpar bit k: parity of P group k's uses so far
     for (SegWalk w = walk0; w.more(); ++si) {
       const Segment sg = w.seg(prm);
       const int jrows = sg.mt * 128 + 128;
-      const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
       const bool e = si == 0 || mbar_wait(bar(kCbEmpty), (si - 1) & 1, ctl);
-      (void)issue_handoff(a && e && !*abort_flag);
+      if (WIDE) {
+        for (int k = 0; k < N / 64; ++k, ++cbk) {
+          const bool a = mbar_wait(bar(kCbK0 + (cbk & 1)), (cbk >> 1) & 1, ctl);
+          (void)issue_handoff(a && e && !*abort_flag);
+        }
+      } else {
+        const bool a = mbar_wait(bar(kCbFull), si & 1, ctl);
+        (void)issue_handoff(a && e && !*abort_flag);
+      }
       for (int hi = 0; hi < sg.nh; ++hi, ++gi) {
         const uint32_t s = gi & 1, use = gi >> 1;
-        const bool h = mbar_wait(bar(kHpFull0 + s), use & 1, ctl);
         const bool y = gi < 2 || mbar_wait(bar(kYEmpty0 + s), (use - 1) & 1, ctl);
-        (void)issue_handoff(h && y && !*abort_flag);
+        if (!WIDE) {
+          const bool h = mbar_wait(bar(kHpFull0 + s), use & 1, ctl);
+          (void)issue_handoff(h && y && !*abort_flag);
+        }
         const bool f = mbar_wait(bar(kXsFull0 + s), use & 1, ctl);
         for (int k = 0; k < jrows / 64; ++k) {
           const bool p = mbar_wait(bar(kPFull0 + k), (gpar >> k) & 1u, ctl);
@@ -587,45 +647,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = gi & 1;
         // this row's cs2 (one coalesced L2 read per warp), fetched while the MMAs finish
         const float cs_i = __ldg(prm.cs2 + ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q + row);
-        // and, for a later state slice, the row of y the earlier slices wrote (a plain load: the
-        // buffer is this kernel's output too)
-        const uint4* prev_row =
-            ACC && int64_t(sg.c) * Q + row < prm.L
-                ? reinterpret_cast<const uint4*>(prm.yacc + ((int64_t(sg.b) * prm.L + int64_t(sg.c) * Q + row) * H + hh) * 64)
-                : nullptr;
-        const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && !*abort_flag;
+        // WIDE: the head's Z rows (2^{cs2_i} C hprev^T, from the readout) in the hprev slot
+        const bool zok = !WIDE || mbar_wait(bar(kHpFull0 + s), (gi >> 1) & 1, ctl);
+        const bool ok = mbar_wait(bar(kYFull0 + s), (gi >> 1) & 1, ctl) && zok && !*abort_flag;
         tc_fence_after();
         if (store_thread) bulk_wait_read0();  // the staging buffer is free again
         named_bar_sync(kBarEpi, 32 * kEpiWarps);
         if (ok) {
           const float e = ex2(cs_i);
           uint8_t* ys = smem + SM::kY + r * 128;
+          const uint8_t* zr = smem + SM::kHp0 + s * SM::kHpBytes + r * 128;
 #pragma unroll
           for (int quarter = 0; quarter < 4; ++quarter) {
             uint32_t a[16], q2[16];
             __syncwarp();
             tmem_ld16(trow + 256 + 128 * s + 16 * quarter, a);
-            tmem_ld16(trow + 256 + 128 * s + 64 + 16 * quarter, q2);
+            if (!WIDE) tmem_ld16(trow + 256 + 128 * s + 64 + 16 * quarter, q2);
             tmem_ld_wait();
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               const int cc = 2 * quarter + c2;
-              // the earlier slices' y (ACC), widened and added before the one rounding
-              uint4 pv = make_uint4(0, 0, 0, 0);
-              if (ACC && prev_row) pv = prev_row[cc];
-              const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
               uint32_t o[4];
+              if (WIDE) {
+                // y = Y1 + Z (Z already carries its decay 2^{cs2_i})
+                const uint4 zv = *reinterpret_cast<const uint4*>(zr + ((cc ^ (r & 7)) << 4));
+                const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
 #pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const int k0 = 8 * c2 + 2 * e2;
-                float2 v2 = fma_f32x2(make_float2(e, e),
-                                      make_float2(__uint_as_float(q2[k0]), __uint_as_float(q2[k0 + 1])),
-                                      make_float2(__uint_as_float(a[k0]), __uint_as_float(a[k0 + 1])));
-                if (ACC) {
-                  v2.x += bf16lo_to_f32(pw[e2]);
-                  v2.y += bf16hi_to_f32(pw[e2]);
+                for (int e2 = 0; e2 < 4; ++e2) {
+                  const int k0 = 8 * c2 + 2 * e2;
+                  o[e2] = pack_bf16x2(__uint_as_float(a[k0]) + bf16lo_to_f32(zw[e2]),
+                                      __uint_as_float(a[k0 + 1]) + bf16hi_to_f32(zw[e2]));
                 }
-                o[e2] = pack_bf16x2(v2.x, v2.y);
+              } else {
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                  const int k0 = 8 * c2 + 2 * e2;
+                  const float2 v2 = fma_f32x2(make_float2(e, e),
+                                              make_float2(__uint_as_float(q2[k0]), __uint_as_float(q2[k0 + 1])),
+                                              make_float2(__uint_as_float(a[k0]), __uint_as_float(a[k0 + 1])));
+                  o[e2] = pack_bf16x2(v2.x, v2.y);
+                }
               }
               *reinterpret_cast<uint4*>(ys + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -633,7 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kYEmpty0 + s));
+        if (lane == 0) {
+          mbar_arrive(bar(kYEmpty0 + s));
+          if (WIDE) mbar_arrive(bar(kHpEmpty0 + s));  // the Z rows have been read
+        }
         fence_proxy_async_smem();
         named_bar_sync(kBarEpi, 32 * kEpiWarps);
         if (store_thread && ok && tile_live) {
@@ -656,10 +720,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NB>
+template <int NB, bool WIDE>
 cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cudaStream_t st) {
   using SM = ScSmem<NB>;
-  auto kern = prm.yacc ? chunk_scan_tc_kernel<NB, true> : chunk_scan_tc_kernel<NB, false>;
+  auto kern = chunk_scan_tc_kernel<NB, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, st, maps[0], maps[1], maps[2], maps[3],
@@ -668,41 +732,25 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
 
 }  // namespace
 
+bool chunk_scan_wide(const Problem& p) { return p.N > 128 && p.N % 64 == 0 && p.N >= p.Q; }
+
 bool chunk_scan_tc_ok(const Problem& p) {
   return p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) &&
-         (p.N == 64 || p.N == 128 || scan_slices(p) > 1) && p.L <= (int64_t(1) << 31) - 1 &&
+         (p.N == 64 || p.N == 128 || chunk_scan_wide(p)) && p.L <= (int64_t(1) << 31) - 1 &&
          p.b * p.nc * p.H * p.P < (int64_t(1) << 31) && p.G * p.N < (int64_t(1) << 31);
 }
 
-cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
-                                       const float* D, const float* cs2, const float* dtT,
-                                       const void* hprev, void* y, const void* yacc, uint32_t* status,
-                                       cudaStream_t st, const char** why, int32_t col0, int32_t width);
-
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
                                  const float* D, const float* cs2, const float* dtT,
-                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
+                                 const void* hprev, void* zbuf, void* y, uint32_t* status, cudaStream_t st,
                                  const char** why) {
-  const int64_t slices = scan_slices(p);
-  // one launch per 128-column slice of the state; each later slice adds the y its predecessors
-  // left (the launches are stream-ordered, and each waits for the previous grid before reading)
-  for (int64_t s = 0; s < slices; ++s) {
-    const int32_t width = slices > 1 ? 128 : static_cast<int32_t>(p.N);
-    const cudaError_t e = launch_chunk_scan_tc_slice(
-        p, x, B, C, s == 0 ? D : nullptr, cs2, dtT, static_cast<const uint16_t*>(hprev) + width * s, y,
-        s == 0 ? nullptr : y, status, st, why, static_cast<int32_t>(width * s), width);
+  const bool wide = chunk_scan_wide(p);
+  if (wide) {
+    // Z = 2^{cs2_i} C hprev^T first, into zbuf (b, L, H, P) bf16
+    const cudaError_t e = launch_chunk_readout_tc(p, C, cs2, hprev, zbuf, status, st, why);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
-}
-
-// One launch over the state columns col0 .. col0 + width - 1 (width 64 or 128); hprev points at
-// column col0 of the full state rows.
-cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const void* B, const void* C,
-                                       const float* D, const float* cs2, const float* dtT,
-                                       const void* hprev, void* y, const void* yacc, uint32_t* status,
-                                       cudaStream_t st, const char** why, int32_t col0, int32_t width) {
-  CUtensorMap maps[5];  // x, B, C, hprev, y
+  CUtensorMap maps[5];  // x, B, C, hprev or Z, y
   const uint64_t xdims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t xstr[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
   const uint64_t bdims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
@@ -710,17 +758,19 @@ cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const vo
   const uint32_t box3[3] = {64, 128, 1};
   // hprev (rows p of each (b, c, h), N columns) as (64 columns, rows, N / 64 column halves), so
   // that one box {64, 64, N / 64} lands as N / 64 swizzled 8 KB tiles
-  const uint64_t hdims[3] = {64, uint64_t(p.b * p.nc * p.H * p.P), uint64_t(width / 64)};
+  const uint64_t hdims[3] = {64, uint64_t(p.b * p.nc * p.H * p.P), uint64_t(wide ? 2 : p.N / 64)};
   const uint64_t hstr[2] = {uint64_t(p.N * 2), 128};
-  const uint32_t hbox[3] = {64, 64, uint32_t(width / 64)};
+  const uint32_t hbox[3] = {64, 64, uint32_t(wide ? 2 : p.N / 64)};
   if (!encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, bdims, bstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
       !encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, bdims, bstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why) ||
-      !encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, hprev, hdims, hstr, hbox,
-                   CU_TENSOR_MAP_SWIZZLE_128B, why) ||
+      !(wide ? encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, zbuf, xdims, xstr, box3,
+                           CU_TENSOR_MAP_SWIZZLE_128B, why)
+             : encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, hprev, hdims, hstr, hbox,
+                           CU_TENSOR_MAP_SWIZZLE_128B, why)) ||
       !encode_tmap(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why))
     return cudaErrorInvalidValue;
@@ -730,8 +780,6 @@ cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const vo
   prm.nc = static_cast<int32_t>(p.nc);
   prm.Q = static_cast<int32_t>(p.Q);
   prm.N = static_cast<int32_t>(p.N);
-  prm.col0 = col0;
-  prm.yacc = static_cast<const uint16_t*>(yacc);
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.MT = static_cast<int32_t>(p.Q / 128);
   prm.units = p.b * p.nc * prm.MT * p.H;
@@ -744,8 +792,9 @@ cudaError_t launch_chunk_scan_tc_slice(const Problem& p, const void* x, const vo
   int sms = num_sms_current_device();
   if (sms <= 0) sms = 1;
   const int grid = static_cast<int>(prm.units < sms ? prm.units : sms);
-  if (width == 64) return launch_nb<1>(maps, prm, grid, st);
-  return launch_nb<2>(maps, prm, grid, st);
+  if (wide) return launch_nb<2, true>(maps, prm, grid, st);
+  if (p.N == 64) return launch_nb<1, false>(maps, prm, grid, st);
+  return launch_nb<2, false>(maps, prm, grid, st);
 }
 
 }  // namespace ssd

@@ -119,7 +119,7 @@ ssd_status step_scan(const ssd::Problem& p, const void* x, const void* B, const 
   cudaError_t e;
   if (use_scan_tc(p)) {
     const char* why = nullptr;
-    e = ssd::launch_chunk_scan_tc(p, x, B, C, D, v.cs2, v.dtT, v.hprev, y, v.status, st, &why);
+    e = ssd::launch_chunk_scan_tc(p, x, B, C, D, v.cs2, v.dtT, v.hprev, v.S, y, v.status, st, &why);
     if (why) return fail(SSD_ERR_CUDA, "chunk_scan: %s", why);
   } else {
     e = ssd::launch_chunk_scan_simt(p, x, B, C, D, v.cs2, v.dtT, v.hprev, y, st);

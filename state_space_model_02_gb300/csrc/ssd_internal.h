@@ -30,17 +30,6 @@ struct Layout {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// The tensor-core chunk_scan keeps C and hprev resident for 64 or 128 state columns.  Larger
-// state sizes (a multiple of 128, up to 512) run it once per 128-column slice -- the products
-// C.B^T and C.hprev^T are sums over the state dimension and the mask and decays act element-wise
-// -- each later slice adding the y of the earlier ones.
-inline int64_t scan_slices(const Problem& p) {
-  return (p.io_bf16 && p.P == 64 && (p.Q == 128 || p.Q == 256) && p.N > 128 && p.N % 128 == 0 &&
-          p.N <= 512)
-             ? p.N / 128
-             : 1;
-}
-
 inline Layout make_layout(const Problem& p) {
   Layout l{};
   const size_t cs_bytes = static_cast<size_t>(p.b * p.H * p.nc * p.Q) * 4u;
@@ -133,10 +122,19 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
                                   const float* dtT, void* S, uint32_t* status, cudaStream_t st,
                                   const char** why);
 
+// States above 128 columns (chunk_scan_wide): the readout kernel computes the term through
+// hprev, Z = 2^{cs2_i} C hprev^T (b, L, H, P) bf16, into zbuf (which needs b * nc * Q * H * P
+// bf16 elements: the S region serves, S being dead after state_passing and no smaller when
+// N >= Q), then chunk_scan adds it.
+bool chunk_scan_wide(const Problem& p);
+bool chunk_readout_tc_ok(const Problem& p);
+cudaError_t launch_chunk_readout_tc(const Problem& p, const void* C, const float* cs2, const void* hprev,
+                                    void* Z, uint32_t* status, cudaStream_t st, const char** why);
+
 cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B, const void* C,
                                  const float* D, const float* cs2, const float* dtT,
-                                 const void* hprev, void* y, uint32_t* status, cudaStream_t st,
-                                 const char** why);
+                                 const void* hprev, void* zbuf, void* y, uint32_t* status,
+                                 cudaStream_t st, const char** why);
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 

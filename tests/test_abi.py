@@ -103,11 +103,13 @@ def test_status_strings(lib):
 def test_kernel_plan(lib):
     assert ssd.kernel_plan(shape()) == 3                              # both steps on tensor cores
     assert ssd.kernel_plan(shape(batch=4, seqlen=2048, nheads=24)) == 3
-    assert ssd.kernel_plan(shape(dstate=256)) & 2                     # sliced tensor-core chunk_scan
+    assert ssd.kernel_plan(shape(dstate=256)) & 2                     # wide tensor-core chunk_scan
     assert ssd.kernel_plan(shape(dstate=384)) & 2
     assert ssd.kernel_plan(shape(dstate=512)) & 2
-    assert not ssd.kernel_plan(shape(dstate=640)) & 2                 # above 512: CUDA-core chunk_scan
-    assert not ssd.kernel_plan(shape(dstate=192)) & 2                 # not a multiple of 128
+    assert ssd.kernel_plan(shape(dstate=640)) & 2
+    assert ssd.kernel_plan(shape(dstate=192, chunk=128)) & 2
+    assert not ssd.kernel_plan(shape(dstate=192)) & 2                 # below the 256-token chunk
+    assert not ssd.kernel_plan(shape(dstate=200)) & 2                 # not a multiple of 64
     assert ssd.kernel_plan(shape(flags=ssd.FLAG_FORCE_SIMT)) == 0
     assert ssd.kernel_plan(shape(io_dtype=ssd.SSD_F32)) == 0          # exact-fp32 CUDA-core path
     assert ssd.kernel_plan(shape(headdim=32)) == 0

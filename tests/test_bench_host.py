@@ -55,12 +55,13 @@ def test_profiled_traffic_only_while_the_kernel_is_unchanged(fake_root):
     assert bench.profiled_traffic("chunk_scan", "some_workload") is None
 
 
-@pytest.mark.parametrize("dstate,plan,launches", [
-    (128, 3, 1),   # one tensor-core launch
-    (256, 3, 2),   # two 128-column slices
-    (512, 3, 4),
-    (512, 1, 1),   # CUDA-core chunk_scan: one launch whatever the state size
-    (64, 0, 1),
+@pytest.mark.parametrize("dstate,chunk,plan,launches", [
+    (128, 256, 3, 1),   # one tensor-core launch
+    (256, 256, 3, 2),   # the readout, then chunk_scan
+    (512, 256, 3, 2),
+    (192, 128, 3, 2),
+    (512, 256, 1, 1),   # CUDA-core chunk_scan: one launch whatever the state size
+    (64, 64, 0, 1),
 ])
-def test_scan_launch_count(dstate, plan, launches):
-    assert bench.scan_launches({"dstate": dstate}, plan) == launches
+def test_scan_launch_count(dstate, chunk, plan, launches):
+    assert bench.scan_launches({"dstate": dstate, "chunk": chunk}, plan) == launches

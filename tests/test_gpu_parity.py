@@ -108,8 +108,9 @@ EDGE = [
     dict(batch=1, seqlen=512, nheads=6, headdim=64, dstate=128, ngroups=2, chunk=256),  # 3 heads per group
     dict(batch=1, seqlen=300, nheads=3, headdim=32, dstate=48, chunk=64),      # CUDA-core path shapes
     dict(batch=1, seqlen=700, nheads=2, headdim=64, dstate=256, chunk=256),
-    dict(batch=2, seqlen=600, nheads=3, headdim=64, dstate=384, chunk=128),   # three state slices
-    dict(batch=1, seqlen=520, nheads=4, headdim=64, dstate=256, ngroups=2, chunk=256),  # slices x groups
+    dict(batch=2, seqlen=600, nheads=3, headdim=64, dstate=384, chunk=128),   # wide state, Q = 128
+    dict(batch=1, seqlen=520, nheads=4, headdim=64, dstate=256, ngroups=2, chunk=256),  # wide x groups
+    dict(batch=1, seqlen=500, nheads=5, headdim=64, dstate=192, chunk=128),   # wide, 3 K steps
 ]
 
 
@@ -219,8 +220,8 @@ def test_tensor_core_and_cuda_core_paths_agree():
 
 
 @pytest.mark.parametrize("n", [256, 512])
-def test_sliced_tensor_core_scan_matches_cuda_core(n):
-    # state sizes above 128 run the tensor-core chunk_scan once per 128-column slice
+def test_wide_tensor_core_scan_matches_cuda_core(n):
+    # state sizes above 128: the readout kernel, then chunk_scan with a K loop over the state
     inp = synth.make_inputs(batch=1, seqlen=1000, nheads=4, headdim=64, dstate=n, chunk=256,
                             io_dtype="bf16", init=True, seed=13)
     y_tc, f_tc = run(inp)
