@@ -67,6 +67,13 @@ typedef enum {
 
 /* Kernel-selection flags (ssd_shape.flags). */
 #define SSD_FLAG_FORCE_SIMT 1u /* use the CUDA-core kernels even where the tensor-core ones apply */
+/* Fail instead of falling back: chunk_state and chunk_scan run on the tensor cores for bf16 I/O
+ * with headdim 64 and chunk 128 or 256 (chunk_state: dstate 64, 128, 256 or 512; chunk_scan:
+ * dstate 64 or 128, or a multiple of 64 above 128 and not below chunk).  Every other shape runs
+ * on the float32 CUDA-core kernels, correctly but several times slower (ssd_kernel_plan tells
+ * which).  With this flag, ssd_fwd, ssd_chunk_state and ssd_chunk_scan return
+ * SSD_ERR_UNSUPPORTED before any launch for such a shape, ssd_last_error() naming the reason. */
+#define SSD_FLAG_REQUIRE_TENSOR_CORES 2u
 
 typedef struct {
   int64_t batch;   /* b  >= 1                                               */

@@ -87,6 +87,26 @@ bool use_scan_tc(const ssd::Problem& p) {
   return !(p.flags & SSD_FLAG_FORCE_SIMT) && ssd::chunk_scan_tc_ok(p);
 }
 
+// Why a step of p would run on the CUDA-core kernels (null: it runs on the tensor cores).
+const char* simt_reason(const ssd::Problem& p, bool scan) {
+  if (p.flags & SSD_FLAG_FORCE_SIMT) return "SSD_FLAG_FORCE_SIMT is set";
+  if (!p.io_bf16) return "float32 I/O";
+  if (p.P != 64) return "headdim is not 64";
+  if (p.Q != 128 && p.Q != 256) return "chunk is not 128 or 256";
+  if (scan ? !ssd::chunk_scan_tc_ok(p) : !ssd::chunk_state_tc_ok(p))
+    return scan ? "dstate is not 64, 128, or a multiple of 64 above 128 and at least chunk"
+                : "dstate is not 64, 128, 256 or 512";
+  return nullptr;
+}
+
+// SSD_FLAG_REQUIRE_TENSOR_CORES: SSD_ERR_UNSUPPORTED when a requested step would fall back.
+ssd_status require_tc(const ssd::Problem& p, bool state, bool scan) {
+  if (!(p.flags & SSD_FLAG_REQUIRE_TENSOR_CORES)) return SSD_OK;
+  const char* why = state ? simt_reason(p, false) : nullptr;
+  if (!why && scan) why = simt_reason(p, true);
+  return why ? fail(SSD_ERR_UNSUPPORTED, "no tensor-core kernel for this shape: %s", why) : SSD_OK;
+}
+
 // ---- the four steps on an already checked problem ----
 
 ssd_status step_cumsum(const ssd::Problem& p, const float* dt, const float* A, const Views& v,
@@ -251,6 +271,7 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   SSD_TRY(maybe(D, "D"));
   SSD_TRY(maybe(init_state, "init_state"));
   SSD_TRY(maybe(final_state, "final_state"));
+  SSD_TRY(require_tc(p, true, true));
   Views v;
   SSD_TRY(carve(p, workspace, workspace_bytes, &v));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -284,6 +305,7 @@ ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* B,
   SSD_TRY(make_problem(shape, &p));
   SSD_TRY(need(x, "x"));
   SSD_TRY(need(B, "B"));
+  SSD_TRY(require_tc(p, true, false));
   Views v;
   SSD_TRY(carve(p, workspace, workspace_bytes, &v));
   return step_state(p, x, B, v, static_cast<cudaStream_t>(stream));
@@ -310,6 +332,7 @@ ssd_status ssd_chunk_scan(const ssd_shape* shape, const void* x, const void* B, 
   SSD_TRY(need(C, "C"));
   SSD_TRY(need(y, "y"));
   SSD_TRY(maybe(D, "D"));
+  SSD_TRY(require_tc(p, false, true));
   Views v;
   SSD_TRY(carve(p, workspace, workspace_bytes, &v));
   return step_scan(p, x, B, C, D, y, v, static_cast<cudaStream_t>(stream));

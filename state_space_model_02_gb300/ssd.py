@@ -6,6 +6,7 @@ first call raises -- there is no fallback.
 """
 import ctypes
 import os
+import warnings
 from dataclasses import dataclass
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -13,6 +14,7 @@ LIB_PATH = os.path.join(HERE, "libssd.so")
 
 SSD_F32, SSD_BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
+FLAG_REQUIRE_TENSOR_CORES = 2   # fail (SSD_ERR_UNSUPPORTED) rather than fall back to the CUDA cores
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_ALIGN",
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_WORKSPACE"}
 
@@ -139,6 +141,23 @@ def workspace_layout(prob: Problem) -> WorkspaceLayout:
     return out
 
 
+_fallback_warned = set()
+
+
+def _warn_cuda_cores(prob: Problem):
+    """Warns once per shape when bf16 work falls back to the float32 CUDA-core kernels."""
+    if prob.io_dtype != SSD_BF16 or prob.flags & (FLAG_FORCE_SIMT | FLAG_REQUIRE_TENSOR_CORES):
+        return
+    key = (prob.headdim, prob.dstate, prob.chunk)
+    if key in _fallback_warned or kernel_plan(prob) == 3:
+        return
+    _fallback_warned.add(key)
+    warnings.warn("ssd.fwd: headdim %d, dstate %d, chunk %d run chunk_state / chunk_scan on the "
+                  "CUDA cores (tensor-core plan %d of 3); pass flags=FLAG_REQUIRE_TENSOR_CORES to "
+                  "make this an error" % (prob.headdim, prob.dstate, prob.chunk, kernel_plan(prob)),
+                  RuntimeWarning, stacklevel=3)
+
+
 def kernel_plan(prob: Problem) -> int:
     """bit 0: chunk_state on tensor cores, bit 1: chunk_scan on tensor cores."""
     return int(load_library().ssd_kernel_plan(ctypes.byref(prob.c_shape())))
@@ -184,6 +203,7 @@ def fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None, final_sta
     torch = _torch()
     prob = problem_of(x, B, chunk, flags)
     b, L, H, P, N, G = prob.batch, prob.seqlen, prob.nheads, prob.headdim, prob.dstate, prob.ngroups
+    _warn_cuda_cores(prob)
     _need(x, "x", x.dtype)
     _need(B, "B", x.dtype, (b, L, G, N))
     _need(C, "C", x.dtype, (b, L, G, N))
@@ -269,6 +289,7 @@ def bwd(x, dt, A, B, C, D, dy, chunk=256, init_state=None, dfinal=None, *, works
     torch = _torch()
     prob = problem_of(x, B, chunk, flags)
     b, L, H, P, N, G = prob.batch, prob.seqlen, prob.nheads, prob.headdim, prob.dstate, prob.ngroups
+    _warn_cuda_cores(prob)
     _need(x, "x", x.dtype)
     _need(B, "B", x.dtype, (b, L, G, N))
     _need(C, "C", x.dtype, (b, L, G, N))

@@ -100,6 +100,18 @@ def test_status_strings(lib):
     assert lib.ssd_status_str(5) == b"on-chip wait timed out"
 
 
+def test_require_tensor_cores_rejects_fallback_shapes_before_launch(lib):
+    # no GPU needed: the check happens on the host before the workspace is even looked at
+    for kw, why in [(dict(headdim=32), b"headdim"), (dict(chunk=64), b"chunk"), (dict(io_dtype=0), b"float32"),
+                    (dict(dstate=48), b"dstate")]:
+        s = shape(flags=ssd.FLAG_REQUIRE_TENSOR_CORES, **kw).c_shape()
+        rc = lib.ssd_fwd(ctypes.byref(s), *([ctypes.c_void_p(16)] * 10), 0, None)
+        assert rc == 2 and why in lib.ssd_last_error(), (kw, rc, lib.ssd_last_error())
+    # a tensor-core shape passes that check and fails later, on the (missing) workspace
+    s = shape(flags=ssd.FLAG_REQUIRE_TENSOR_CORES).c_shape()
+    assert lib.ssd_fwd(ctypes.byref(s), *([ctypes.c_void_p(16)] * 10), 0, None) == 6
+
+
 def test_kernel_plan(lib):
     assert ssd.kernel_plan(shape()) == 3                              # both steps on tensor cores
     assert ssd.kernel_plan(shape(batch=4, seqlen=2048, nheads=24)) == 3

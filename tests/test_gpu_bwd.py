@@ -1,9 +1,9 @@
 """Parity of the backward pass (ssd_bwd) with the float64 adjoint oracle (oracle/ref_bwd.py).
 
 Metric per gradient: max|got - ref| / max|ref|.  Bounds: 1e-4 with float32 I/O (every scan runs
-in float32 there); with bf16 I/O the scans' inputs and outputs are bf16, so 3e-2 for the
-gradients that pass through one scan (dx, dB, dC, dinit, dD) and 5e-2 for ddt and dA, which
-combine two scans' outputs (<dy, y> - dt <x, g B>, then a sum over the sequence).
+in float32 there) and 2e-2 with bf16 I/O, the forward's bounds.  Measured with bf16 on GB300
+(the 130M layer, every gradient over the whole tensor): dx 2.8e-3, dB 4.6e-3, dC 3.6e-3,
+dA 7.4e-5, ddt 7.1e-6, dD 1.3e-7 -- the two scans that feed ddt and dA run in float32.
 """
 import numpy as np
 import pytest
@@ -47,8 +47,8 @@ def run_case(dtype, b, L, H, P, N, G, chunk, init=True, with_dfinal=True, seed=0
     torch.cuda.synchronize()
     dy_ref = synth.bf16_bits_to_f32(dy_host) if dtype == "bf16" else dy32
     ref = recurrence_bwd_np(inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.init, dy_ref, dfin)
-    tol = tol or (1e-4 if dtype == "f32" else 3e-2)
-    tol_sc = tol_sc or (1e-4 if dtype == "f32" else 5e-2)
+    tol = tol or (1e-4 if dtype == "f32" else 2e-2)
+    tol_sc = tol_sc or (1e-4 if dtype == "f32" else 2e-2)
     errs = {}
     for name in ("dx", "dB", "dC", "dD", "ddt", "dA") + (("dinit",) if init else ()):
         got = g[name].float().cpu().numpy()
@@ -69,11 +69,20 @@ def test_f32_no_init_no_dfinal():
 
 @pytest.mark.parametrize("G", [1, 2])
 def test_bf16_tensor_core_shapes(G):
-    # P = 64, N = 128, chunk 256: the adjoint scan runs on the tensor-core kernels, the two
-    # role-swapped scans (head dim 128) on the CUDA-core ones; 600 tokens: a ragged last chunk
+    # P = 64, N = 128, chunk 256: the forward-again and adjoint scans in float32 (CUDA cores),
+    # the role-swapped scans as head-dim-64 scans on the tensor cores; 600 tokens: ragged end
     run_case("bf16", 2, 600, 4, 64, 128, G, 256, seed=7 + G)
 
 
 def test_bf16_state_64_all_tensor_core():
     # N = 64: the role-swapped scans have head dim 64 and state 64, tensor-core shapes too
     run_case("bf16", 1, 512, 4, 64, 64, 1, 256, seed=11)
+
+
+@pytest.mark.slow
+def test_bf16_mamba2_130m_layer_full():
+    # the 130M layer as the bench times it (b4 L2048 H24 P64 N128 G1, chunk 256, no init), every
+    # gradient against the float64 adjoint over the whole tensor
+    errs = run_case("bf16", 4, 2048, 24, 64, 128, 1, 256, init=False, seed=19)
+    assert max(errs.values()) > 0.0
+
