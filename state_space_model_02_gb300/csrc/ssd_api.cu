@@ -111,7 +111,7 @@ ssd_status require_tc(const ssd::Problem& p, bool state, bool scan) {
 
 ssd_status step_cumsum(const ssd::Problem& p, const float* dt, const float* A, const Views& v,
                        cudaStream_t st, bool unit_scale = false) {
-  const cudaError_t e = ssd::launch_chunk_cumsum(p, dt, A, v.cs2, v.dtT, st, unit_scale);
+  const cudaError_t e = ssd::launch_chunk_cumsum(p, dt, A, v.cs2, v.dtT, v.status, st, unit_scale);
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_cumsum launch");
 }
 

@@ -68,8 +68,11 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // ---- launchers (each returns the launch's cudaError_t; none synchronises) ----
 
+// chunk_cumsum stages dt tiles by TMA when chunk_cumsum_tma_ok (rows 16-byte aligned); its
+// bounded waits report SSD_ERR_TIMEOUT in *status.
+bool chunk_cumsum_tma_ok(const Problem& p, const float* dt);
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
-                                float* dtT, cudaStream_t st, bool unit_scale = false);
+                                float* dtT, uint32_t* status, cudaStream_t st, bool unit_scale = false);
 
 cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,

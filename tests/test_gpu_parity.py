@@ -133,11 +133,29 @@ def test_persistent_chunk_state_shapes(shape):
     check_against_oracle(inp)
 
 
-def test_cumsum_32_head_tiles():
-    # H a multiple of 32 and enough chunks: chunk_cumsum stages 32 heads per CTA (whole
-    # 128-byte rows of dt); ragged last chunk
-    inp = synth.make_inputs(batch=1, seqlen=19520 + 37, nheads=32, headdim=16, dstate=16, chunk=64,
+@pytest.mark.parametrize("nheads,seqlen,chunk", [
+    (32, 19520 + 37, 64), (48, 13056 + 101, 128),                        # one CTA per tile
+    (32, 38912 + 37, 64), (16, 77824 + 5, 128), (8, 38912 + 61, 64),     # TMA-staged, persistent
+], ids=["tile32_q64", "tile16_q128", "tma_tile32_q64", "tma_tile16_q128", "tma_tile8_q64"])
+def test_cumsum_wide_head_tiles(nheads, seqlen, chunk):
+    # chunk_cumsum with 32, 16 or 8 heads per tile (runs of 8 tokens per lane; 2 for 8 heads of a
+    # 64-token chunk), in the one-CTA-per-tile kernel and, with four or more tiles per SM, the
+    # persistent TMA kernel; ragged last chunk.  cs2 and dt checked directly, then y.
+    inp = synth.make_inputs(batch=1, seqlen=seqlen, nheads=nheads, headdim=16, dstate=16, chunk=chunk,
                             io_dtype="f32", init=True, seed=17)
+    t = to_device(inp)
+    prob = ssd.problem_of(t["x"], t["B"], chunk)
+    ws = ssd.alloc_workspace(prob)
+    ssd.chunk_cumsum(prob, t["dt"], t["A"], ws)
+    torch.cuda.synchronize()
+    cs2, dtT = [v.float().cpu().numpy() for v in ssd.intermediates(prob, ws)[:2]]
+    cs2_ref, dt_ref = ref.cumsum_log2(inp.dt, inp.A, chunk)
+    assert rel(cs2, cs2_ref) <= 1e-6
+    assert np.array_equal(dtT, dt_ref.astype(np.float32))
+    # padded tokens of the last chunk repeat its last token's value exactly
+    n_last = seqlen - (-(-seqlen // chunk) - 1) * chunk
+    last = cs2[:, :, -1, :]
+    assert np.array_equal(last[..., n_last:], np.repeat(last[..., n_last - 1:n_last], chunk - n_last, axis=-1))
     check_against_oracle(inp)
 
 
