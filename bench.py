@@ -72,6 +72,12 @@ def algorithmic_bwd(shape):
     st = b * H * P * N * 4
     return 3 * b * L * H * P * e + 4 * b * L * G * N * e + 2 * b * L * H * 4 + 2 * st + (st if shape["init"] else 0)
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
+KERNELS_FUSED = ("chunk_cumsum", "fwd_pass_state", "chunk_scan")   # chunk_state + state_passing in one
+
+
+def step_kernels(plan):
+    """The kernels of one forward step for an ssd_kernel_plan value (bit 2: fused fwd_pass_state)."""
+    return KERNELS_FUSED if plan >= 0 and plan & 4 else KERNELS
 
 
 def parse():
@@ -105,16 +111,20 @@ def algorithmic(shape):
         "chunk_state": b * L * H * P * e + b * L * G * N * e + 2 * cs + st * e,
         "state_passing": st * e + b * H * nc * 4 + st * e + 2 * b * H * P * N * 4,
         "chunk_scan": 2 * b * L * H * P * e + 2 * b * L * G * N * e + 2 * cs + st * e + H * 4,
+        # the fused kernel: x, B, cs2 / dtT in, hprev and the final state out (S stays on chip)
+        "fwd_pass_state": b * L * H * P * e + b * L * G * N * e + 2 * cs + st * e + b * H * P * N * 4,
     }
     fl = {
         "chunk_cumsum": 2 * b * L * H,
         "chunk_state": 2 * b * nc * H * Q * P * N,
         "state_passing": 2 * st,
+        "fwd_pass_state": 2 * b * nc * H * Q * P * N + 2 * st,
         "chunk_scan": (2 * b * nc * G * (Q * (Q + 1) // 2) * N + 2 * b * nc * H * (Q * (Q + 1) // 2) * P
                        + 2 * b * nc * H * Q * P * N),
     }
     if shape["init"]:
         by["state_passing"] += b * H * P * N * 4
+        by["fwd_pass_state"] += b * H * P * N * 4
     return by, fl
 
 
@@ -132,6 +142,7 @@ def source_digest(kernel):
     """Digest of a kernel's source file with comments and whitespace removed: a profile stays
     valid across comment edits and is dropped by any change to the code."""
     files = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state_tc.cu",
+             "fwd_pass_state": "chunk_state_tc.cu",
              "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan_tc.cu",
              "decode": "decode.cu", "selective_scan": "selective_scan.cu"}
     p = os.path.join(ROOT, "state_space_model_02_gb300", "csrc", files[kernel])
@@ -490,27 +501,29 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        # one ssd_fwd call: chunk_cumsum, chunk_state, state_passing, chunk_scan, launched back
-        # to back
+        # one ssd_fwd call: chunk_cumsum, chunk_state and state_passing (one fused fwd_pass_state
+        # kernel where the plan says so), chunk_scan, launched back to back
         ssd.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk=inp.chunk, init_state=d["init"],
                 y=y, final_state=fin, workspace=wsbuf, stream=stream)
 
+    plan = ssd.kernel_plan(prob)
+    kernels = step_kernels(plan)
+
     def step_by_kernel(evs):
-        # the same four launches through the per-step entry points, an event between launches
+        # the same launches through the per-step entry points, an event between launches
+        calls = {
+            "chunk_cumsum": lambda: ssd.chunk_cumsum(prob, d["dt"], d["A"], wsbuf, stream),
+            "chunk_state": lambda: ssd.chunk_state(prob, d["x"], d["B"], wsbuf, stream),
+            "state_passing": lambda: ssd.state_passing(prob, d["init"], fin, wsbuf, stream),
+            "fwd_pass_state": lambda: ssd.fwd_pass_state(prob, d["x"], d["B"], d["init"], fin, wsbuf, stream),
+            "chunk_scan": lambda: ssd.chunk_scan(prob, d["x"], d["B"], d["C"], d["D"], y, wsbuf, stream),
+        }
+        for i, n in enumerate(kernels):
+            if evs:
+                evs[i].record(stream)
+            calls[n]()
         if evs:
-            evs[0].record(stream)
-        ssd.chunk_cumsum(prob, d["dt"], d["A"], wsbuf, stream)
-        if evs:
-            evs[1].record(stream)
-        ssd.chunk_state(prob, d["x"], d["B"], wsbuf, stream)
-        if evs:
-            evs[2].record(stream)
-        ssd.state_passing(prob, d["init"], fin, wsbuf, stream)
-        if evs:
-            evs[3].record(stream)
-        ssd.chunk_scan(prob, d["x"], d["B"], d["C"], d["D"], y, wsbuf, stream)
-        if evs:
-            evs[4].record(stream)
+            evs[len(kernels)].record(stream)
 
     for k in range(max(3, args.warmup)):
         flush_l2(k)
@@ -541,14 +554,14 @@ def run_ours(args):
     totals = [e[0].elapsed_time(e[1]) for e in step_evs]
     ms_step = float(np.sum(totals) / args.steps)
     # per-kernel durations (for the roofline): the same steps again with an event between kernels
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush_l2(k)
         step_by_kernel(evs[k])
     torch.cuda.synchronize()
-    per_kernel = {n: [] for n in KERNELS}
+    per_kernel = {n: [] for n in kernels}
     for e in evs:
-        for i, n in enumerate(KERNELS):
+        for i, n in enumerate(kernels):
             per_kernel[n].append(e[i].elapsed_time(e[i + 1]))
     ms_step = max_over_ranks(ms_step, ws, dist, dev)
     tokens = prob.batch * prob.seqlen
@@ -558,17 +571,17 @@ def run_ours(args):
     by, fl = algorithmic(shape)
     peaks = load_peaks()
     kern = {}
-    for n in KERNELS:
+    for n in kernels:
         ms = float(np.mean(per_kernel[n]))
         t_hbm = by[n] / (peaks["hbm"] * 1e9)
-        t_ten = fl[n] / (peaks["bf16"] * 1e12) if n in ("chunk_state", "chunk_scan") else 0.0
+        t_ten = fl[n] / (peaks["bf16"] * 1e12) if n in ("chunk_state", "fwd_pass_state", "chunk_scan") else 0.0
         bound = "hbm" if t_hbm >= t_ten else "tensor"
         ach = by[n] / (ms * 1e-3) / 1e9 if bound == "hbm" else fl[n] / (ms * 1e-3) / 1e12
         peak = peaks["hbm"] if bound == "hbm" else peaks["bf16"]
         kern[n] = {"us": 1e3 * ms, "share": ms / ms_step, "bound": bound, "achieved": ach, "peak": peak,
                    "frac": ach / peak, "alg_bytes": by[n], "alg_flops": fl[n],
                    "tensor_frac_of_peak": fl[n] / (ms * 1e-3) / 1e12 / peaks["bf16"]}
-    dom = max(KERNELS, key=lambda n: kern[n]["us"])
+    dom = max(kernels, key=lambda n: kern[n]["us"])
     kd = kern[dom]
     tr = profiled_traffic(dom, args.workload)
     roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"], "peak": kd["peak"],
@@ -600,7 +613,6 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(inp, args.cpu_seconds)
-    plan = ssd.kernel_plan(prob)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
@@ -609,12 +621,13 @@ def run_ours(args):
         "config": {"workload": args.workload, **shape,
                    "l2": "flushed before every step (256 MiB write + 256 MiB read, outside the timed events)",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "tensor_core_steps": {"chunk_state": bool(plan & 1), "chunk_scan": bool(plan & 2)}},
+                   "tensor_core_steps": {"chunk_state": bool(plan & 1), "chunk_scan": bool(plan & 2),
+                                         "fused_fwd_pass_state": bool(plan & 4)}},
         "roofline": roofline,
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in kern[n].items()}
-                    for n in KERNELS},
+                    for n in kernels},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": (len(KERNELS) - 1 + scan_launches(shape, plan)) * args.steps,
+        "gpu_launches": (len(kernels) - 1 + scan_launches(shape, plan)) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -74,6 +74,15 @@ typedef enum {
  * which).  With this flag, ssd_fwd, ssd_chunk_state and ssd_chunk_scan return
  * SSD_ERR_UNSUPPORTED before any launch for such a shape, ssd_last_error() naming the reason. */
 #define SSD_FLAG_REQUIRE_TENSOR_CORES 2u
+/* fwd_pass_state ("Mamba-2 cuda-tile forward pass kernels", section 2, second kernel): for bf16
+ * I/O, headdim 64, chunk 128 or 256 and dstate 64 or 128, one kernel can compute the chunk states
+ * and chain them: a CTA walks one (batch, head pair) chain chunk by chunk with the chain's float32
+ * state in tensor memory, writing hprev and final_state; S never reaches memory and state_passing
+ * does not run.  It keeps one SM per chain and was slower than the two kernels on every workload
+ * measured, so ssd_fwd and ssd_fwd_pass_state run it only with SSD_FLAG_FUSED_STATE (where the
+ * shape allows it); SSD_FLAG_SEPARATE_STATE_PASSING (the default behaviour) wins if both are set. */
+#define SSD_FLAG_SEPARATE_STATE_PASSING 4u
+#define SSD_FLAG_FUSED_STATE 8u
 
 typedef struct {
   int64_t batch;   /* b  >= 1                                               */
@@ -148,6 +157,14 @@ ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* B,
 ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state,
                              float* final_state, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* Steps 2 and 3 together, fwd_pass_state (same page, section 2, second kernel): the fused
+ * kernel with SSD_FLAG_FUSED_STATE where the shape allows it, else ssd_chunk_state then
+ * ssd_state_passing.  Reads cs2/dtT, x, B, init_state (may be null: zero); writes hprev and
+ * (if non-null) final_state, float32 (b, H, P, N).  The fused kernel leaves S unwritten. */
+ssd_status ssd_fwd_pass_state(const ssd_shape* shape, const void* x, const void* B,
+                              const float* init_state, float* final_state, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /* Step 4, chunk_scan (same page, section 2, compute_out):
  * y_i = sum_{j<=i in chunk} exp2(cs2_i - cs2_j) dt_j (C_i.B_j) x_j
@@ -282,8 +299,9 @@ const char* ssd_status_str(ssd_status status);
 const char* ssd_last_error(void);
 
 /* Which kernel family ssd_fwd would use for each step of `shape`:
- * bit 0 chunk_state on tensor cores, bit 1 chunk_scan on tensor cores.
- * -1 for an invalid shape. */
+ * bit 0 chunk_state on tensor cores, bit 1 chunk_scan on tensor cores, bit 2 chunk_state and
+ * state_passing as the one fused fwd_pass_state kernel (SSD_FLAG_FUSED_STATE).  -1 for an
+ * invalid shape. */
 int ssd_kernel_plan(const ssd_shape* shape);
 
 #ifdef __cplusplus

@@ -42,8 +42,11 @@ constexpr uint32_t kBarScale = 1, kBarEpi = 2;  // named barriers of the scale a
 struct CsParams {
   int32_t L, H, nc, Q, N, hpg, pairs_per_group, n_tiles;
   int64_t items;
+  int64_t chains;            // fused kernel: (batch, head pair, n-tile) chains, each nc items
   const float* cs2;
   const float* dtT;
+  const float* init;         // fused kernel: state before the first chunk (b, H, P, N), or null
+  float* final_state;        // fused kernel: state after the last chunk (b, H, P, N), or null
   uint32_t* status;
   uint64_t wait_ns;
 };
@@ -90,17 +93,58 @@ __device__ __forceinline__ Item item_at(int64_t i, const CsParams& prm) {
   return it;
 }
 
+// Chunk c of chain ch; chains run (n-tile fastest, head pair, batch).
+__device__ __forceinline__ Item chain_item(int64_t ch, int c, const CsParams& prm) {
+  Item it;
+  const int64_t per_b = int64_t(prm.H / prm.hpg) * prm.pairs_per_group * prm.n_tiles;
+  const int64_t b = ch / per_b;
+  const int rem = static_cast<int>(ch - b * per_b);
+  it.nt = rem % prm.n_tiles;
+  const int pair = rem / prm.n_tiles;
+  it.g = pair / prm.pairs_per_group;
+  it.h0 = it.g * prm.hpg + 2 * (pair % prm.pairs_per_group);
+  it.nh = min(2, (it.g + 1) * prm.hpg - it.h0);
+  it.c = c;
+  it.b = static_cast<int>(b);
+  return it;
+}
+
+// The CTA's j-th work item; false past its last.  Separate kernels: items i = blockIdx.x +
+// j * gridDim.x.  Fused: chains ch = blockIdx.x + (j / nc) * gridDim.x, each walked through its
+// chunks in order (c = j % nc), so the chain's state can be carried from one item to the next.
+template <bool FUSED>
+__device__ __forceinline__ bool local_item(uint32_t j, const CsParams& prm, Item& it) {
+  if (!FUSED) {
+    const int64_t i = blockIdx.x + int64_t(j) * gridDim.x;
+    if (i >= prm.items) return false;
+    it = item_at(i, prm);
+    return true;
+  }
+  const uint32_t nc = static_cast<uint32_t>(prm.nc);
+  const int64_t ch = blockIdx.x + int64_t(j / nc) * gridDim.x;
+  if (ch >= prm.chains) return false;
+  it = chain_item(ch, static_cast<int>(j % nc), prm);
+  return true;
+}
+
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
   return pack_bf16x2(bf16lo_to_f32(v) * w, bf16hi_to_f32(v) * w);
 }
 
-template <int NT>
+// FUSED: fwd_pass_state in one kernel -- instead of storing S, the epilogue carries each chain's
+// float32 state in tensor memory (h <- 2^{cs2_last} h + S_c, chunk by chunk), stores the state
+// entering every chunk as hprev (bf16, through tm_S, which then maps hprev) and the state after
+// the last chunk as final_state.
+template <int NT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_B,
                           const __grid_constant__ CUtensorMap tm_S, const CsParams prm) {
   using SM = CsSmem<NT>;
   constexpr int S = SM::kStages;
+  // two accumulators, and for the fused kernel the chain's state after them
+  constexpr uint32_t kCols = FUSED ? 4 * NT : 2 * NT;
+  static_assert(!FUSED || NT <= 128, "the fused kernel keeps three NT-column regions in tensor memory");
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -132,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), 2 * NT);
+    tmem_alloc(smem_u32(tmem_slot), kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -140,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{prm.wait_ns, abort_flag, prm.status};
-  const int64_t i0 = blockIdx.x, istep = gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -151,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gk = 0, it_local = 0;
       // x and B are inputs of the step: the first item's k-blocks are requested before waiting
       // for the previous kernel (cs2 / dtT come from it)
-      const int pre = i0 < prm.items ? (kblocks < S ? kblocks : S) : 0;
+      Item it0;
+      const int pre = local_item<FUSED>(0, prm, it0) ? (kblocks < S ? kblocks : S) : 0;
       auto load_kb = [&](const Item& it, int kb, uint32_t k) {
         const int s = static_cast<int>(k % S);
         const uint32_t st = sb + s * SM::kStage, full = bar(SM::kFull + s);
@@ -162,13 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pend_full[s] = true;
         ph_full[s] = (k / S) & 1;
       };
-      if (pre > 0) {
-        const Item it = item_at(i0, prm);
-        for (int kb = 0; kb < pre; ++kb) load_kb(it, kb, uint32_t(kb));
-      }
+      for (int kb = 0; kb < pre; ++kb) load_kb(it0, kb, uint32_t(kb));
       grid_dep_wait();
-      for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
-        const Item it = item_at(i, prm);
+      for (;; ++it_local) {
+        Item it;
+        if (!local_item<FUSED>(it_local, prm, it)) break;
         const uint32_t ws = it_local & 1;
         if (it_local >= 2) (void)mbar_wait(bar(SM::kWinEmpty + ws), ((it_local >> 1) - 1) & 1, ctl);
         if (!*abort_flag) {
@@ -199,7 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, NT, 1, 1);
     uint32_t gk = 0, it_local = 0;
-    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
+    for (;; ++it_local) {
+      Item it;
+      if (!local_item<FUSED>(it_local, prm, it)) break;
       const uint32_t a = it_local & 1;
       if (it_local >= 2) (void)mbar_wait(bar(SM::kAccEmpty + a), ((it_local >> 1) - 1) & 1, ctl);
       for (int kb = 0; kb < kblocks; ++kb, ++gk) {
@@ -230,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- decay weights, x~ = w x in place
     const int ts = threadIdx.x - 32 * kScaleWarp0;  // 0..127
     uint32_t gk = 0, it_local = 0;
-    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
-      const Item it = item_at(i, prm);
+    for (;; ++it_local) {
+      Item it;
+      if (!local_item<FUSED>(it_local, prm, it)) break;
       const uint32_t ws = it_local & 1;
       const bool have = mbar_wait(bar(SM::kWinFull + ws), (it_local >> 1) & 1, ctl);
       const float* win = reinterpret_cast<const float*>(smem + SM::kWin + ws * SM::kWinBytes);
@@ -269,15 +314,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(SM::kScaled + s));
       }
     }
+  } else if (FUSED) {
+    // ------------- epilogue (fused): hprev = h, then h <- 2^{cs2_last} h + S, chunk by chunk
+    const int q4 = warp & 3, r = 32 * q4 + lane;  // TMEM lane quarter; accumulator row = (head, p)
+    const int k = r >> 6, pr = r & 63;
+    const bool store_thread = warp == kEpiWarp0 && lane == 0;
+    const uint32_t hcol = tmem + 2 * NT + (uint32_t(32 * q4) << 16);  // this warp's rows of h
+    grid_dep_wait();  // cs2 comes from the previous kernel; hprev may still be read by older ones
+    for (uint32_t it_local = 0;; ++it_local) {
+      Item it;
+      if (!local_item<FUSED>(it_local, prm, it)) break;
+      const uint32_t a = it_local & 1;
+      const bool row_ok = k < it.nh;
+      const int64_t bh = int64_t(it.b) * prm.H + it.h0 + k;  // (batch, head) of this row
+      // the chunk's decay, requested before the accumulator wait so that its latency hides
+      const float dec = row_ok ? ex2(__ldg(prm.cs2 + (bh * prm.nc + it.c) * Q + Q - 1)) : 0.f;
+      const bool ok = mbar_wait(bar(SM::kAccFull + a), (it_local >> 1) & 1, ctl) && !*abort_flag;
+      tc_fence_after();
+      if (store_thread) bulk_wait_read0();  // the staging buffer is free again
+      named_bar_sync(kBarEpi, 128);
+      if (ok) {
+        const int64_t row = (bh * 64 + pr) * prm.N + it.nt * NT;  // (b, h, p, n-tile) in init / final
+        const float* init_row = it.c == 0 && row_ok && prm.init ? prm.init + row : nullptr;
+        float* fin_row = it.c == prm.nc - 1 && row_ok && prm.final_state ? prm.final_state + row : nullptr;
+#pragma unroll 1
+        for (int q = 0; q < NT / 32; ++q) {
+          uint32_t sv[32], hv[32];
+          __syncwarp();
+          tmem_ld32(tmem + a * NT + (uint32_t(32 * q4) << 16) + q * 32, sv);
+          if (it.c > 0) tmem_ld32(hcol + q * 32, hv);  // it.c is uniform over the warp
+          tmem_ld_wait();
+          if (it.c == 0) {  // the chain starts from init (zero without one)
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 f = init_row ? __ldg(reinterpret_cast<const float4*>(init_row + q * 32 + j))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+              hv[j] = __float_as_uint(f.x);
+              hv[j + 1] = __float_as_uint(f.y);
+              hv[j + 2] = __float_as_uint(f.z);
+              hv[j + 3] = __float_as_uint(f.w);
+            }
+          }
+          // hprev of this chunk (the state entering it) in bf16 into the staging box
+          uint8_t* box = smem + SM::kOut + ((q >> 1) * 2 + k) * kBox;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int cc = (q & 1) * 4 + c4;
+            *reinterpret_cast<uint4*>(box + pr * 128 + ((cc ^ (pr & 7)) << 4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(hv[8 * c4]), __uint_as_float(hv[8 * c4 + 1])),
+                           pack_bf16x2(__uint_as_float(hv[8 * c4 + 2]), __uint_as_float(hv[8 * c4 + 3])),
+                           pack_bf16x2(__uint_as_float(hv[8 * c4 + 4]), __uint_as_float(hv[8 * c4 + 5])),
+                           pack_bf16x2(__uint_as_float(hv[8 * c4 + 6]), __uint_as_float(hv[8 * c4 + 7])));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            hv[j] = __float_as_uint(fmaf(dec, __uint_as_float(hv[j]), __uint_as_float(sv[j])));
+          tmem_st32(hcol + q * 32, hv);
+          if (fin_row) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(fin_row + q * 32 + j) =
+                  make_float4(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1]), __uint_as_float(hv[j + 2]),
+                              __uint_as_float(hv[j + 3]));
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SM::kAccEmpty + a));
+      fence_proxy_async_smem();
+      named_bar_sync(kBarEpi, 128);
+      if (store_thread && ok) {
+        for (int j = 0; j < NT / 64; ++j)
+          for (int kk = 0; kk < it.nh; ++kk)
+            tma_store_2d(&tm_S, sb + SM::kOut + (j * 2 + kk) * kBox, it.nt * NT + j * 64,
+                         ((it.b * prm.nc + it.c) * prm.H + it.h0 + kk) * 64);
+        bulk_commit();
+      }
+    }
+    if (store_thread) bulk_wait_read0();  // the stores have read the staging buffer
   } else {
     // --------------------------------- epilogue: accumulator -> bf16 -> TMA store of S
     const int q4 = warp & 3, r = 32 * q4 + lane;  // TMEM lane quarter; accumulator row = (head, p)
     const int k = r >> 6, pr = r & 63;
     const bool store_thread = warp == kEpiWarp0 && lane == 0;
-    uint32_t it_local = 0;
     grid_dep_wait();  // S may still be read by the kernels before the previous one
-    for (int64_t i = i0; i < prm.items; i += istep, ++it_local) {
-      const Item it = item_at(i, prm);
+    for (uint32_t it_local = 0;; ++it_local) {
+      Item it;
+      if (!local_item<FUSED>(it_local, prm, it)) break;
       const uint32_t a = it_local & 1;
       const bool ok = mbar_wait(bar(SM::kAccFull + a), (it_local >> 1) & 1, ctl) && !*abort_flag;
       tc_fence_after();
@@ -324,20 +449,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * NT);
+    tmem_dealloc(tmem, kCols);
   }
 }
 
-template <int NT>
+template <int NT, bool FUSED = false>
 cudaError_t launch_nt(const CUtensorMap& tx, const CUtensorMap& tb, const CUtensorMap& ts,
                       const CsParams& prm, cudaStream_t st) {
   using SM = CsSmem<NT>;
-  auto kern = chunk_state_tc_kernel<NT>;
+  auto kern = chunk_state_tc_kernel<NT, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   int sms = num_sms_current_device();
   if (sms <= 0) sms = 1;
-  const int64_t grid = prm.items < sms ? prm.items : sms;
+  const int64_t units = FUSED ? prm.chains : prm.items;
+  const int64_t grid = units < sms ? units : sms;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), SM::kAlloc, st, tx, tb, ts, prm);
 }
 
@@ -570,11 +696,12 @@ bool chunk_state_tc_ok(const Problem& p) {
          p.L <= (int64_t(1) << 31) - 1 && p.b * p.nc * p.H * p.P < (int64_t(1) << 31);
 }
 
-cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
-                                  const float* dtT, void* S, uint32_t* status, cudaStream_t st,
-                                  const char** why) {
-  const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
-  CUtensorMap tx, tb, ts;
+namespace {
+
+// Tensor maps and parameters shared by the chunk_state launches.  out: S, or hprev for the fused
+// kernel (the same (b, nc, H, P, N) bf16 layout).
+bool encode_cs_maps(const Problem& p, int NT, const void* x, const void* B, void* out, CUtensorMap* tx,
+                    CUtensorMap* tb, CUtensorMap* ts, const char** why) {
   // TMA boxes cost about the same for 8 and 16 KB, so each k-block takes one box for x and one
   // for B: x (b, L, H, P) viewed as (p, token, head, batch) with a box of two heads, and B
   // (b, L, G, N) as (64 columns, token, N / 64 column blocks, batch) with a box of NT / 64 blocks;
@@ -583,27 +710,31 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
     const uint64_t dims[4] = {64, uint64_t(p.L), uint64_t(p.H), uint64_t(p.b)};
     const uint64_t strides[3] = {uint64_t(p.H * p.P * 2), uint64_t(p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
     const uint32_t box[4] = {64, 64, 2, 1};
-    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
+    if (!encode_tmap(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
-      return cudaErrorInvalidValue;
+      return false;
   }
   {
     const uint64_t dims[4] = {64, uint64_t(p.L), uint64_t(p.G * p.N / 64), uint64_t(p.b)};
     const uint64_t strides[3] = {uint64_t(p.G * p.N * 2), 128, uint64_t(p.L * p.G * p.N * 2)};
     const uint32_t box[4] = {64, 64, uint32_t(NT / 64), 1};
-    if (!encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, B, dims, strides, box,
+    if (!encode_tmap(tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, B, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
-      return cudaErrorInvalidValue;
+      return false;
   }
   {
     const uint64_t dims[2] = {uint64_t(p.N), uint64_t(p.b * p.nc * p.H * p.P)};
     const uint64_t strides[1] = {uint64_t(p.N * 2)};
     const uint32_t box[2] = {64, 64};
-    if (!encode_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, S, dims, strides, box,
+    if (!encode_tmap(ts, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
-      return cudaErrorInvalidValue;
+      return false;
   }
-  CsParams prm;
+  return true;
+}
+
+CsParams make_cs_params(const Problem& p, int NT, const float* cs2, const float* dtT, uint32_t* status) {
+  CsParams prm{};
   prm.L = static_cast<int32_t>(p.L);
   prm.H = static_cast<int32_t>(p.H);
   prm.nc = static_cast<int32_t>(p.nc);
@@ -612,11 +743,24 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
   prm.hpg = static_cast<int32_t>(p.hpg);
   prm.pairs_per_group = static_cast<int32_t>((p.hpg + 1) / 2);
   prm.n_tiles = static_cast<int32_t>(p.N / NT);
-  prm.items = p.b * p.nc * p.G * prm.pairs_per_group * prm.n_tiles;
+  prm.chains = p.b * p.G * prm.pairs_per_group * prm.n_tiles;
+  prm.items = prm.chains * p.nc;
   prm.cs2 = cs2;
   prm.dtT = dtT;
   prm.status = status;
   prm.wait_ns = kWaitLimitNs;
+  return prm;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,
+                                  const float* dtT, void* S, uint32_t* status, cudaStream_t st,
+                                  const char** why) {
+  const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
+  CUtensorMap tx, tb, ts;
+  if (!encode_cs_maps(p, NT, x, B, S, &tx, &tb, &ts, why)) return cudaErrorInvalidValue;
+  const CsParams prm = make_cs_params(p, NT, cs2, dtT, status);
   // the persistent kernel once every SM gets a dozen items or more, one CTA per item below that
   int sms = num_sms_current_device();
   if (sms <= 0) sms = 1;
@@ -634,6 +778,23 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
     }
   }
   return cudaErrorInvalidValue;
+}
+
+bool chunk_state_fused_ok(const Problem& p) {
+  return chunk_state_tc_ok(p) && (p.N == 64 || p.N == 128);
+}
+
+cudaError_t launch_chunk_state_fused(const Problem& p, const void* x, const void* B, const float* cs2,
+                                     const float* dtT, const float* init, void* hprev, float* final_state,
+                                     uint32_t* status, cudaStream_t st, const char** why) {
+  if (!chunk_state_fused_ok(p)) return cudaErrorInvalidValue;
+  const int NT = static_cast<int>(p.N);
+  CUtensorMap tx, tb, th;
+  if (!encode_cs_maps(p, NT, x, B, hprev, &tx, &tb, &th, why)) return cudaErrorInvalidValue;
+  CsParams prm = make_cs_params(p, NT, cs2, dtT, status);
+  prm.init = init;
+  prm.final_state = final_state;
+  return NT == 64 ? launch_nt<64, true>(tx, tb, th, prm, st) : launch_nt<128, true>(tx, tb, th, prm, st);
 }
 
 }  // namespace ssd

@@ -134,6 +134,29 @@ ssd_status step_passing(const ssd::Problem& p, const float* init, float* final_s
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "state_passing launch");
 }
 
+// fwd_pass_state as one kernel, on request only.  It runs one CTA per (batch, head pair) chain,
+// and a CTA of chunk_state's pipeline moves a chunk's x and B at about the per-SM share of HBM
+// bandwidth, so with fewer chains than SMs the separate chunk_state (over every (chunk, head
+// pair)) and state_passing finish first on every workload measured.
+bool use_fused_state(const ssd::Problem& p) {
+  return use_state_tc(p) && ssd::chunk_state_fused_ok(p) && (p.flags & SSD_FLAG_FUSED_STATE) &&
+         !(p.flags & SSD_FLAG_SEPARATE_STATE_PASSING);
+}
+
+// chunk_state + state_passing, fused where use_fused_state says so.
+ssd_status step_state_passing(const ssd::Problem& p, const void* x, const void* B, const float* init,
+                              float* final_state, const Views& v, cudaStream_t st) {
+  if (!use_fused_state(p)) {
+    const ssd_status s1 = step_state(p, x, B, v, st);
+    return s1 != SSD_OK ? s1 : step_passing(p, init, final_state, v, st);
+  }
+  const char* why = nullptr;
+  const cudaError_t e = ssd::launch_chunk_state_fused(p, x, B, v.cs2, v.dtT, init, v.hprev, final_state,
+                                                      v.status, st, &why);
+  if (why) return fail(SSD_ERR_CUDA, "fwd_pass_state: %s", why);
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "fwd_pass_state launch");
+}
+
 ssd_status step_scan(const ssd::Problem& p, const void* x, const void* B, const void* C,
                      const float* D, void* y, const Views& v, cudaStream_t st) {
   cudaError_t e;
@@ -278,8 +301,7 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   const cudaError_t e = cudaMemsetAsync(v.status, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   SSD_TRY(step_cumsum(p, dt, A, v, st));
-  SSD_TRY(step_state(p, x, B, v, st));
-  SSD_TRY(step_passing(p, init_state, final_state, v, st));
+  SSD_TRY(step_state_passing(p, x, B, init_state, final_state, v, st));
   SSD_TRY(step_scan(p, x, B, C, D, y, v, st));
   g_last_error[0] = '\0';
   return SSD_OK;
@@ -320,6 +342,21 @@ ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state, fl
   Views v;
   SSD_TRY(carve(p, workspace, workspace_bytes, &v));
   return step_passing(p, init_state, final_state, v, static_cast<cudaStream_t>(stream));
+}
+
+ssd_status ssd_fwd_pass_state(const ssd_shape* shape, const void* x, const void* B,
+                              const float* init_state, float* final_state, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  ssd::Problem p;
+  SSD_TRY(make_problem(shape, &p));
+  SSD_TRY(need(x, "x"));
+  SSD_TRY(need(B, "B"));
+  SSD_TRY(maybe(init_state, "init_state"));
+  SSD_TRY(maybe(final_state, "final_state"));
+  SSD_TRY(require_tc(p, true, false));
+  Views v;
+  SSD_TRY(carve(p, workspace, workspace_bytes, &v));
+  return step_state_passing(p, x, B, init_state, final_state, v, static_cast<cudaStream_t>(stream));
 }
 
 ssd_status ssd_chunk_scan(const ssd_shape* shape, const void* x, const void* B, const void* C,
@@ -618,7 +655,7 @@ const char* ssd_last_error(void) { return g_last_error; }
 int ssd_kernel_plan(const ssd_shape* shape) {
   ssd::Problem p;
   if (make_problem(shape, &p) != SSD_OK) return -1;
-  return (use_state_tc(p) ? 1 : 0) | (use_scan_tc(p) ? 2 : 0);
+  return (use_state_tc(p) ? 1 : 0) | (use_scan_tc(p) ? 2 : 0) | (use_fused_state(p) ? 4 : 0);
 }
 
 }  // extern "C"

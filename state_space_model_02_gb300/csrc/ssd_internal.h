@@ -125,6 +125,17 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
                                   const float* dtT, void* S, uint32_t* status, cudaStream_t st,
                                   const char** why);
 
+// fwd_pass_state in one kernel (chunk_state's persistent kernel walking whole chains, each
+// chain's float32 state kept in tensor memory): writes hprev and final_state directly, no S and
+// no state_passing launch.  Shapes: chunk_state_fused_ok (the tensor-core chunk_state shapes with
+// N <= 128); it uses one CTA per (batch, head pair) chain.  Selected only on request
+// (SSD_FLAG_FUSED_STATE): with one SM per chain it is slower than the two kernels on the
+// workloads measured.
+bool chunk_state_fused_ok(const Problem& p);
+cudaError_t launch_chunk_state_fused(const Problem& p, const void* x, const void* B, const float* cs2,
+                                     const float* dtT, const float* init, void* hprev, float* final_state,
+                                     uint32_t* status, cudaStream_t st, const char** why);
+
 // States above 128 columns (chunk_scan_wide): the readout kernel computes the term through
 // hprev, Z = 2^{cs2_i} C hprev^T (b, L, H, P) bf16, into zbuf (which needs b * nc * Q * H * P
 // bf16 elements: the S region serves, S being dead after state_passing and no smaller when

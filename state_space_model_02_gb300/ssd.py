@@ -15,12 +15,14 @@ LIB_PATH = os.path.join(HERE, "libssd.so")
 SSD_F32, SSD_BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_REQUIRE_TENSOR_CORES = 2   # fail (SSD_ERR_UNSUPPORTED) rather than fall back to the CUDA cores
+FLAG_SEPARATE_STATE_PASSING = 4  # chunk_state and state_passing as two kernels (the default)
+FLAG_FUSED_STATE = 8             # the fused fwd_pass_state kernel wherever the shape allows it
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_ALIGN",
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_WORKSPACE"}
 
 # Every entry point of include/ssd.h, in declaration order.
 EXPORTS = ("ssd_workspace_bytes", "ssd_get_workspace_layout", "ssd_fwd", "ssd_chunk_cumsum",
-           "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_read_status",
+           "ssd_chunk_state", "ssd_state_passing", "ssd_fwd_pass_state", "ssd_chunk_scan", "ssd_read_status",
            "ssd_selftest_wait_timeout", "ssd_fwd_noalloc", "ssd_decode", "ssd_selective_scan",
            "ssd_bwd_workspace_bytes", "ssd_bwd",
            "ssd_status_str", "ssd_last_error", "ssd_kernel_plan")
@@ -68,6 +70,7 @@ def load_library(path: str = LIB_PATH):
         "ssd_chunk_cumsum": ([sp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_chunk_state": ([sp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_state_passing": ([sp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "ssd_fwd_pass_state": ([sp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_chunk_scan": ([sp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "ssd_read_status": ([vp, vp], ctypes.c_int),
         "ssd_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ctypes.c_int),
@@ -149,17 +152,18 @@ def _warn_cuda_cores(prob: Problem):
     if prob.io_dtype != SSD_BF16 or prob.flags & (FLAG_FORCE_SIMT | FLAG_REQUIRE_TENSOR_CORES):
         return
     key = (prob.headdim, prob.dstate, prob.chunk)
-    if key in _fallback_warned or kernel_plan(prob) == 3:
+    if key in _fallback_warned or kernel_plan(prob) & 3 == 3:
         return
     _fallback_warned.add(key)
     warnings.warn("ssd.fwd: headdim %d, dstate %d, chunk %d run chunk_state / chunk_scan on the "
                   "CUDA cores (tensor-core plan %d of 3); pass flags=FLAG_REQUIRE_TENSOR_CORES to "
-                  "make this an error" % (prob.headdim, prob.dstate, prob.chunk, kernel_plan(prob)),
+                  "make this an error" % (prob.headdim, prob.dstate, prob.chunk, kernel_plan(prob) & 3),
                   RuntimeWarning, stacklevel=3)
 
 
 def kernel_plan(prob: Problem) -> int:
-    """bit 0: chunk_state on tensor cores, bit 1: chunk_scan on tensor cores."""
+    """bit 0: chunk_state on tensor cores, bit 1: chunk_scan on tensor cores, bit 2: the fused
+    fwd_pass_state kernel (chunk_state + state_passing in one; with FLAG_FUSED_STATE)."""
     return int(load_library().ssd_kernel_plan(ctypes.byref(prob.c_shape())))
 
 
@@ -329,6 +333,13 @@ def state_passing(prob, init_state, final_state, workspace, stream=None):
     _check(load_library().ssd_state_passing(ctypes.byref(prob.c_shape()), _p(init_state),
                                             _p(final_state), _p(workspace), workspace.numel(),
                                             _stream(stream)))
+
+
+def fwd_pass_state(prob, x, B, init_state, final_state, workspace, stream=None):
+    """chunk_state + state_passing: one fused kernel where it applies, else the two steps."""
+    _check(load_library().ssd_fwd_pass_state(ctypes.byref(prob.c_shape()), _p(x), _p(B), _p(init_state),
+                                             _p(final_state), _p(workspace), workspace.numel(),
+                                             _stream(stream)))
 
 
 def chunk_scan(prob, x, B, C, D, y, workspace, stream=None):

@@ -127,6 +127,15 @@ def test_kernel_plan(lib):
     assert ssd.kernel_plan(shape(headdim=32)) == 0
     assert ssd.kernel_plan(shape(chunk=64)) == 0
     assert ssd.kernel_plan(shape(chunk=100)) == -1
+    # fused fwd_pass_state: only with its flag, where the shape allows it (N <= 128); SEPARATE
+    # wins over FUSED
+    fused, sep = ssd.FLAG_FUSED_STATE, ssd.FLAG_SEPARATE_STATE_PASSING
+    assert ssd.kernel_plan(shape(flags=fused)) == 7
+    assert ssd.kernel_plan(shape(dstate=64, flags=fused)) == 7
+    assert ssd.kernel_plan(shape(dstate=256, flags=fused)) == 3
+    assert ssd.kernel_plan(shape(chunk=64, flags=fused)) == 0
+    assert ssd.kernel_plan(shape(flags=fused | sep)) == 3
+    assert ssd.kernel_plan(shape()) & 4 == 0
 
 
 def test_selftest_rejects_bad_limits(lib):

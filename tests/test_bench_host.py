@@ -65,3 +65,17 @@ def test_profiled_traffic_only_while_the_kernel_is_unchanged(fake_root):
 ])
 def test_scan_launch_count(dstate, chunk, plan, launches):
     assert bench.scan_launches({"dstate": dstate, "chunk": chunk}, plan) == launches
+
+
+def test_step_kernels_follow_the_plan():
+    assert bench.step_kernels(3) == ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")
+    assert bench.step_kernels(7) == ("chunk_cumsum", "fwd_pass_state", "chunk_scan")
+    assert bench.step_kernels(0) == bench.KERNELS
+    by, fl = bench.algorithmic(dict(batch=2, seqlen=8192, nheads=80, headdim=64, dstate=128, ngroups=1,
+                                    chunk=256, io_dtype="bf16", init=False))
+    # the fused kernel moves chunk_state's inputs and state_passing's outputs, not S
+    st = 2 * 32 * 80 * 64 * 128 * 2
+    assert by["fwd_pass_state"] == by["chunk_state"] + 2 * 80 * 64 * 128 * 4
+    # what fusing saves: S written and read back, and state_passing's own cs2 and extra state bytes
+    assert by["chunk_state"] + by["state_passing"] - by["fwd_pass_state"] == \
+        2 * st + 2 * 80 * 32 * 4 + 2 * 80 * 64 * 128 * 4

@@ -159,6 +159,52 @@ def test_cumsum_wide_head_tiles(nheads, seqlen, chunk):
     check_against_oracle(inp)
 
 
+FUSED_SHAPES = [
+    dict(batch=2, seqlen=1000, nheads=6, headdim=64, dstate=128, chunk=256),             # ragged
+    dict(batch=1, seqlen=100, nheads=4, headdim=64, dstate=64, chunk=256),               # one chunk
+    dict(batch=2, seqlen=384, nheads=5, headdim=64, dstate=128, chunk=128),              # odd H, Q 128
+    dict(batch=1, seqlen=1536, nheads=6, headdim=64, dstate=128, ngroups=2, chunk=256),  # 3 heads / group
+    dict(batch=3, seqlen=2300, nheads=8, headdim=64, dstate=64, ngroups=2, chunk=128),
+]
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES)
+@pytest.mark.parametrize("init", [True, False])
+def test_fused_fwd_pass_state(shape, init):
+    # chunk_state + state_passing as one kernel (forced): y and the final state against the oracle
+    inp = synth.make_inputs(io_dtype="bf16", init=init, seed=29, **shape)
+    y, fin = run(inp, flags=ssd.FLAG_FUSED_STATE, init=init)
+    b, L, H, P = inp.x.shape
+    pairs = [(bb, hh) for bb in range(b) for hh in range(H)]
+    out = oracle_pairs(inp, pairs)
+    assert rel(gather_y(y, pairs), out["y"]) <= 2e-2
+    assert rel(np.stack([fin[bb, hh] for bb, hh in pairs]), out["final"]) <= 2e-2
+
+
+@pytest.mark.parametrize("flags", [ssd.FLAG_FUSED_STATE, ssd.FLAG_SEPARATE_STATE_PASSING])
+def test_fwd_pass_state_entry_point(flags):
+    # ssd_fwd_pass_state fused or as two kernels: hprev (the state entering every chunk) and the
+    # final state against the oracle's chunk inputs; the separate path's S against its chunk states
+    inp = synth.make_inputs(batch=2, seqlen=1100, nheads=6, headdim=64, dstate=128, ngroups=2, chunk=256,
+                            io_dtype="bf16", init=True, seed=31)
+    t = to_device(inp)
+    prob = ssd.problem_of(t["x"], t["B"], 256, flags)
+    ws = ssd.alloc_workspace(prob)
+    fin = torch.empty(2, 6, 64, 128, device="cuda")
+    ssd.chunk_cumsum(prob, t["dt"], t["A"], ws)
+    ssd.fwd_pass_state(prob, t["x"], t["B"], t["init"], fin, ws)
+    assert ssd.read_status(ws) == 0
+    assert bool(ssd.kernel_plan(prob) & 4) == (flags == ssd.FLAG_FUSED_STATE)
+    _, _, S, hprev = [v.float().cpu().numpy() for v in ssd.intermediates(prob, ws)]
+    pairs = [(b, h) for b in range(2) for h in range(6)]
+    out = oracle_pairs(inp, pairs, want_chunk_in=True)
+    assert rel(np.stack([hprev[b, :, h] for b, h in pairs]), out["chunk_in"]) <= 1e-2
+    assert rel(np.stack([fin.cpu().numpy()[b, h] for b, h in pairs]), out["final"]) <= 1e-2
+    if flags == ssd.FLAG_SEPARATE_STATE_PASSING:
+        S_ref = ref.chunk_states(inp.x, inp.dt, inp.A, inp.B, 256)      # every (b, h) in order
+        assert rel(np.stack([S[b, :, h] for b, h in pairs]), S_ref) <= 1e-2
+
+
 def test_slow_decay_exercises_state_passing():
     # |A| in [0.001, 0.05]: the state carries across many chunks
     inp = synth.make_inputs(batch=1, seqlen=4096, nheads=4, headdim=64, dstate=128, chunk=256,
