@@ -125,6 +125,15 @@ enum : int {
   kCbK0, kCbK1, kCbKEmpty0, kCbKEmpty1  // WIDE: the two (C, B) K-step slots of the CB phase
 };
 
+// The producer warms L2 with the inputs of the head this many heads ahead in the segment (x rows,
+// hprev or Z, cs2 / dt rows).  A head's x and hprev slots free only when the head two places
+// earlier has finished its MMAs, and a load issued then takes about as long from HBM as a head
+// does on the SM (measured: 1.4-1.8 us for x, 2-2.7 us for hprev at 256K tokens), which left the
+// mask waiting for its head's inputs; from L2 the same loads arrive in time.  Measured steps
+// (256K tokens / 2.7B layer): no prefetch 1361 / 225 us, 2 heads ahead 1292 / 211 us, 3 ahead
+// 1304 / 212, 4 ahead 1326 / 213, 6 ahead 1382 / 222.
+constexpr int kPrefetchAhead = 2;
+
 // Work weights of the two 128-row m-tiles of a 256-token chunk (the second one's causal
 // width is twice the first's, but its measured cost per head is about 1.5x, since loads and
 // handoffs, not the mask and MMA work, dominate a unit).
@@ -348,6 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jb = 0; jb < jrows / 128; ++jb)
           tma_load_3d(xs + SM::kXsX + jb * kBox128, &tm_x, xb, hh * 64, sg.c * Q + jb * 128, sg.b);
       };
+      // L2 prefetch of head hh's inputs (no shared memory, no barrier); hprev / Z, cs2 and dt come
+      // from the previous kernels, so this runs only after grid_dep_wait
+      auto prefetch_head = [&](const Segment& sg, int hh) {
+        const int i0 = sg.mt * 128, jrows = i0 + 128;
+        for (int jb = 0; jb < jrows / 128; ++jb) tma_prefetch_3d(&tm_x, hh * 64, sg.c * Q + jb * 128, sg.b);
+        if (WIDE)
+          tma_prefetch_3d(&tm_h, hh * 64, sg.c * Q + i0, sg.b);
+        else
+          tma_prefetch_3d(&tm_h, 0, ((sg.b * prm.nc + sg.c) * H + hh) * 64, 0);
+        const int64_t crow = ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q;
+        bulk_prefetch_l2(prm.cs2 + crow, jrows * 4);
+        bulk_prefetch_l2(prm.dtT + crow, jrows * 4);
+      };
       // C, B and x are inputs of the step, not written by the kernels before this one (and every
       // kernel before the previous one has completed): the first segment's C and B and the first
       // two heads' x are requested before waiting for the previous kernels
@@ -402,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend_xs[s] = true;
             ph_xs[s] = use & 1;
           }
+          if (kPrefetchAhead > 0 && hi + kPrefetchAhead < sg.nh && !*abort_flag)
+            prefetch_head(sg, hh + kPrefetchAhead);
         }
         w.advance(sg.nh, prm);
       }

@@ -202,6 +202,12 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t c0, in
                : "memory");
 }
 
+// Warm L2 with a contiguous range (16-byte aligned, bytes % 16 == 0); no shared memory, no barrier.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // Untiled bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
