@@ -33,30 +33,63 @@ __device__ __forceinline__ void stf(uint16_t* p, int64_t i, float v) {
   p[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
+// The layout kernels below run one block per (batch, token) row group: the block index gives
+// (b, t) once per thread, and the positions inside the group split with 32-bit arithmetic
+// (a shift when the divisor is a power of two) instead of 64-bit division per element.
+struct RowSplit {
+  uint32_t d;
+  int sh;  // log2(d) when d is a power of two, else -1
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return sh >= 0 ? n >> sh : n / d; }
+};
+inline RowSplit row_split(int64_t d) {
+  RowSplit r{static_cast<uint32_t>(d), -1};
+  if (d > 0 && (d & (d - 1)) == 0) {
+    r.sh = 0;
+    while ((int64_t(1) << r.sh) < d) ++r.sh;
+  }
+  return r;
+}
+constexpr int kRowThreads = 128;
+
 // dst[b, t, h, :] = src[b, flip ? L-1-t : t, h / rep, v0 : v0 + vec_dst], in 16-byte vectors
 // (source rows of vec_src vectors, destination rows of vec_dst)
-__global__ void flip_expand_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t L,
-                                   int64_t Hsrc, int64_t Hdst, int64_t vec_src, int64_t vec_dst, int64_t v0,
-                                   bool flip, int64_t total) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const int64_t v = i % vec_dst, row = i / vec_dst;
-  const int64_t h = row % Hdst, bt = row / Hdst, t = bt % L, b = bt / L;
+__global__ void __launch_bounds__(kRowThreads) flip_expand_kernel(
+    const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t L, int64_t Hsrc, int64_t Hdst,
+    int64_t vec_src, int64_t vec_dst, int64_t v0, bool flip, RowSplit by_vec, RowSplit by_rep) {
+  const int64_t bt = blockIdx.x, b = bt / L, t = bt - b * L;
   const int64_t ts = flip ? L - 1 - t : t;
-  const int64_t hs = h / (Hdst / Hsrc);
-  dst[i] = __ldg(src + ((b * L + ts) * Hsrc + hs) * vec_src + v0 + v);
+  const uint4* srow = src + (b * L + ts) * Hsrc * vec_src + v0;
+  uint4* drow = dst + bt * Hdst * vec_dst;
+  const uint32_t n = static_cast<uint32_t>(Hdst * vec_dst);
+  for (uint32_t j = threadIdx.x; j < n; j += kRowThreads) {
+    const uint32_t h = by_vec.div(j), v = j - h * static_cast<uint32_t>(vec_dst);
+    drow[j] = __ldg(srow + int64_t(by_rep.div(h)) * vec_src + v);
+  }
 }
 
-// float32 copy: dst[b, t, h, f] = src[b, flip ? L-1-t : t, h / rep, f], src float32 or bf16
+// float32 copy: dst[b, t, h, f] = src[b, flip ? L-1-t : t, h / rep, f], src float32 or bf16;
+// four consecutive f per thread (F a multiple of 4)
 template <typename IN>
-__global__ void widen_flip_expand_kernel(const IN* __restrict__ src, float* __restrict__ dst, int64_t L,
-                                         int64_t Hsrc, int64_t Hdst, int64_t F, bool flip, int64_t total) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const int64_t f = i % F, row = i / F;
-  const int64_t h = row % Hdst, bt = row / Hdst, t = bt % L, b = bt / L;
+__global__ void __launch_bounds__(kRowThreads) widen_flip_expand_kernel(
+    const IN* __restrict__ src, float* __restrict__ dst, int64_t L, int64_t Hsrc, int64_t Hdst, int64_t F,
+    bool flip, RowSplit by_quads, RowSplit by_rep) {
+  const int64_t bt = blockIdx.x, b = bt / L, t = bt - b * L;
   const int64_t ts = flip ? L - 1 - t : t;
-  dst[i] = ldf(src, ((b * L + ts) * Hsrc + h / (Hdst / Hsrc)) * F + f);
+  const IN* srow = src + (b * L + ts) * Hsrc * F;
+  float* drow = dst + bt * Hdst * F;
+  const uint32_t quads = static_cast<uint32_t>(F / 4), n = static_cast<uint32_t>(Hdst) * quads;
+  for (uint32_t j = threadIdx.x; j < n; j += kRowThreads) {
+    const uint32_t h = by_quads.div(j), f = 4 * (j - h * quads);
+    const IN* sp = srow + int64_t(by_rep.div(h)) * F + f;
+    float4 o;
+    if constexpr (sizeof(IN) == 2) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(sp));
+      o = make_float4(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x), bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+    } else {
+      o = __ldg(reinterpret_cast<const float4*>(sp));
+    }
+    *reinterpret_cast<float4*>(drow + int64_t(h) * F + f) = o;
+  }
 }
 
 // the decay steps of the reversed scan: step t of the reversed sequence decays by dt of
@@ -186,22 +219,28 @@ __global__ void sum_batches_kernel(const float* __restrict__ part, float* __rest
 
 // out[b, t, g, n] = sum over the heads h of group g of scale(b, t, h) y[b, t', h, n], with
 // t' = L-1-t when flip and scale = dt when given (else 1)
-// (y has Nk columns per row; out has N, of which n0 .. n0 + Nk - 1 are written)
+// (y has Nk columns per row; out has N, of which n0 .. n0 + Nk - 1 are written); one block per
+// (b, t)
 template <typename IO>
-__global__ void group_sum_kernel(const IO* __restrict__ y, const float* __restrict__ dt, IO* __restrict__ out,
-                                 int64_t L, int64_t H, int64_t G, int64_t N, int64_t n0, int64_t Nk, bool flip,
-                                 int64_t total) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const int64_t n = i % Nk, r = i / Nk, g = r % G, bt = r / G, t = bt % L, b = bt / L;
-  const int64_t hpg = H / G, ts = flip ? L - 1 - t : t;
-  float s = 0.f;
-  for (int64_t k = 0; k < hpg; ++k) {
-    const int64_t h = g * hpg + k;
-    const float sc = dt ? __ldg(dt + (b * L + t) * H + h) : 1.f;
-    s = fmaf(sc, ldf(y, ((b * L + ts) * H + h) * Nk + n), s);
+__global__ void __launch_bounds__(kRowThreads) group_sum_kernel(
+    const IO* __restrict__ y, const float* __restrict__ dt, IO* __restrict__ out, int64_t L, int64_t H, int64_t G,
+    int64_t N, int64_t n0, int64_t Nk, bool flip, RowSplit by_nk) {
+  const int64_t bt = blockIdx.x, b = bt / L, t = bt - b * L;
+  const int64_t ts = flip ? L - 1 - t : t;
+  const int64_t hpg = H / G;
+  const IO* yrow = y + (b * L + ts) * H * Nk;
+  const float* drow = dt ? dt + bt * H : nullptr;
+  const uint32_t n_out = static_cast<uint32_t>(G * Nk);
+  for (uint32_t j = threadIdx.x; j < n_out; j += kRowThreads) {
+    const uint32_t g = by_nk.div(j), n = j - g * static_cast<uint32_t>(Nk);
+    float s = 0.f;
+    for (int64_t k = 0; k < hpg; ++k) {
+      const int64_t h = g * hpg + k;
+      const float sc = drow ? __ldg(drow + h) : 1.f;
+      s = fmaf(sc, ldf(yrow, h * Nk + n), s);
+    }
+    stf(out, (bt * G + g) * N + n0 + n, s);
   }
-  stf(out, r * N + n0 + n, s);
 }
 
 // dinit = a_0 g_0 = exp(A dt_0) times the reverse scan's final state
@@ -220,10 +259,11 @@ inline unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n
 cudaError_t launch_flip_expand(const void* src, void* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
                                int64_t src_row_bytes, int64_t col_byte0, int64_t dst_row_bytes, bool flip,
                                cudaStream_t st) {
-  const int64_t total = b * L * Hdst * (dst_row_bytes / 16);
-  flip_expand_kernel<<<blocks_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                             L, Hsrc, Hdst, src_row_bytes / 16, dst_row_bytes / 16,
-                                                             col_byte0 / 16, flip, total);
+  const int64_t vec_dst = dst_row_bytes / 16;
+  if (b * L == 0 || Hdst * vec_dst == 0) return cudaSuccess;
+  flip_expand_kernel<<<static_cast<unsigned>(b * L), kRowThreads, 0, st>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), L, Hsrc, Hdst, src_row_bytes / 16, vec_dst,
+      col_byte0 / 16, flip, row_split(vec_dst), row_split(Hdst / Hsrc));
   return cudaGetLastError();
 }
 
@@ -258,13 +298,15 @@ cudaError_t launch_bwd_combine(const Problem& p, const void* dy, const void* x, 
 
 cudaError_t launch_widen_flip_expand(const void* src, float* dst, int64_t b, int64_t L, int64_t Hsrc, int64_t Hdst,
                                      int64_t F, bool flip, bool src_bf16, cudaStream_t st) {
-  const int64_t total = b * L * Hdst * F;
+  if (b * L == 0 || Hdst * F == 0) return cudaSuccess;
+  if (F % 4 != 0) return cudaErrorInvalidValue;  // headdim and dstate are multiples of 16 here
+  const unsigned grid = static_cast<unsigned>(b * L);
   if (src_bf16)
-    widen_flip_expand_kernel<uint16_t><<<blocks_for(total, 256), 256, 0, st>>>(
-        static_cast<const uint16_t*>(src), dst, L, Hsrc, Hdst, F, flip, total);
+    widen_flip_expand_kernel<uint16_t><<<grid, kRowThreads, 0, st>>>(
+        static_cast<const uint16_t*>(src), dst, L, Hsrc, Hdst, F, flip, row_split(F / 4), row_split(Hdst / Hsrc));
   else
-    widen_flip_expand_kernel<float><<<blocks_for(total, 256), 256, 0, st>>>(static_cast<const float*>(src), dst, L,
-                                                                            Hsrc, Hdst, F, flip, total);
+    widen_flip_expand_kernel<float><<<grid, kRowThreads, 0, st>>>(
+        static_cast<const float*>(src), dst, L, Hsrc, Hdst, F, flip, row_split(F / 4), row_split(Hdst / Hsrc));
   return cudaGetLastError();
 }
 
@@ -281,13 +323,15 @@ cudaError_t launch_bwd_scalars(const Problem& p, const float* dfinal, const floa
 
 cudaError_t launch_group_sum(const Problem& p, const void* y, const float* dt, void* out, int64_t n0, int64_t Nk,
                              bool flip, cudaStream_t st) {
-  const int64_t total = p.b * p.L * p.G * Nk;
+  if (p.b * p.L == 0 || p.G * Nk == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(p.b * p.L);
   if (p.io_bf16)
-    group_sum_kernel<uint16_t><<<blocks_for(total, 256), 256, 0, st>>>(
-        static_cast<const uint16_t*>(y), dt, static_cast<uint16_t*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip, total);
+    group_sum_kernel<uint16_t><<<grid, kRowThreads, 0, st>>>(
+        static_cast<const uint16_t*>(y), dt, static_cast<uint16_t*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip,
+        row_split(Nk));
   else
-    group_sum_kernel<float><<<blocks_for(total, 256), 256, 0, st>>>(
-        static_cast<const float*>(y), dt, static_cast<float*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip, total);
+    group_sum_kernel<float><<<grid, kRowThreads, 0, st>>>(
+        static_cast<const float*>(y), dt, static_cast<float*>(out), p.L, p.H, p.G, p.N, n0, Nk, flip, row_split(Nk));
   return cudaGetLastError();
 }
 
