@@ -762,9 +762,7 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
   if (!encode_cs_maps(p, NT, x, B, S, &tx, &tb, &ts, why)) return cudaErrorInvalidValue;
   const CsParams prm = make_cs_params(p, NT, cs2, dtT, status);
   // the persistent kernel once every SM gets a dozen items or more, one CTA per item below that
-  int sms = num_sms_current_device();
-  if (sms <= 0) sms = 1;
-  if (prm.items >= kPersistentItemsPerSm * int64_t(sms)) {
+  if (chunk_state_tc_persistent(p)) {
     switch (NT) {
       case 64: return launch_nt<64>(tx, tb, ts, prm, st);
       case 128: return launch_nt<128>(tx, tb, ts, prm, st);
@@ -778,6 +776,14 @@ cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B
     }
   }
   return cudaErrorInvalidValue;
+}
+
+bool chunk_state_tc_persistent(const Problem& p) {
+  const int NT = p.N >= 256 ? 256 : static_cast<int>(p.N);
+  const int64_t items = p.b * p.nc * p.G * ((p.hpg + 1) / 2) * (p.N / NT);
+  int sms = num_sms_current_device();
+  if (sms <= 0) sms = 1;
+  return items >= kPersistentItemsPerSm * int64_t(sms);
 }
 
 bool chunk_state_fused_ok(const Problem& p) {

@@ -43,12 +43,14 @@ inline Layout make_layout(const Problem& p) {
   return l;
 }
 
-// Launches `kern` on `st` with programmatic stream serialization: the kernel may begin (its
-// prologue: barrier init, tensor-memory allocation, tensor-map prefetch) while the previous
-// kernel in the stream is finishing, and waits in grid_dep_wait() before touching global memory.
+// Launches `kern` on `st`, with programmatic stream serialization when `pdl`: the kernel may
+// begin (its prologue: barrier init, tensor-memory allocation, tensor-map prefetch) while the
+// previous kernel in the stream is finishing, and waits in grid_dep_wait() before touching
+// global memory.  Without it the launch waits for the previous kernel as usual, and the
+// kernel's grid_dep_wait / grid_dep_launch do nothing.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args... args) {
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -57,10 +59,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  return launch_kernel(true, kern, grid, block, smem, st, args...);
 }
 
 // Default limit of one bounded on-chip wait (ns).
@@ -74,9 +81,10 @@ bool chunk_cumsum_tma_ok(const Problem& p, const float* dt);
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* cs2,
                                 float* dtT, uint32_t* status, cudaStream_t st, bool unit_scale = false);
 
+// pdl: launch with programmatic dependent launch (see launch_kernel).
 cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,
-                                 cudaStream_t st);
+                                 cudaStream_t st, bool pdl = true);
 
 cudaError_t launch_chunk_state_simt(const Problem& p, const void* x, const void* B, const float* cs2,
                                     const float* dtT, void* S, cudaStream_t st);
@@ -119,6 +127,8 @@ cudaError_t launch_decode(const Problem& p, const void* x, const float* dt, cons
 
 // Tensor-core (tcgen05) kernels.  Applicability is decided by the *_tc_ok predicates.
 bool chunk_state_tc_ok(const Problem& p);
+// Whether launch_chunk_state_tc runs its persistent kernel for p (many items per SM).
+bool chunk_state_tc_persistent(const Problem& p);
 bool chunk_scan_tc_ok(const Problem& p);
 
 cudaError_t launch_chunk_state_tc(const Problem& p, const void* x, const void* B, const float* cs2,

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(256) state_passing_scalar_kernel(
 
 cudaError_t launch_state_passing(const Problem& p, const void* S, const float* cs2,
                                  const float* init, void* hprev, float* final_state,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool pdl) {
   const int64_t PN = p.P * p.N;
   if (p.io_bf16 && PN % 8 == 0) {
     const int64_t total8 = p.b * p.H * (PN / 8);
@@ -237,12 +237,12 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
     const auto Sb = static_cast<const uint16_t*>(S);
     const auto hb = static_cast<uint16_t*>(hprev);
     if (ctas_per_sm <= 4)
-      return launch_pdl(state_passing_bf16x8_kernel<16, true, 4>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+      return launch_kernel(pdl, state_passing_bf16x8_kernel<16, true, 4>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
                         cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
     if (ctas_per_sm <= 12)
-      return launch_pdl(state_passing_bf16x8_kernel<8, false, 12>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+      return launch_kernel(pdl, state_passing_bf16x8_kernel<8, false, 12>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
                         cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
-    return launch_pdl(state_passing_bf16x8_kernel<4, false, 18>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
+    return launch_kernel(pdl, state_passing_bf16x8_kernel<4, false, 18>, dim3(blocks8), dim3(kBf16x8Threads), 0, st, Sb,
                       cs2, init, hb, final_state, p.H, PN, p.nc, p.Q, total8);
   }
   const bool vec = (PN % 4) == 0;
@@ -250,17 +250,17 @@ cudaError_t launch_state_passing(const Problem& p, const void* S, const float* c
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
   if (vec) {
     if (p.io_bf16)
-      return launch_pdl(state_passing_vec4_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
+      return launch_kernel(pdl, state_passing_vec4_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
                         init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
-      return launch_pdl(state_passing_vec4_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
+      return launch_kernel(pdl, state_passing_vec4_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
                         init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   } else {
     if (p.io_bf16)
-      return launch_pdl(state_passing_scalar_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
+      return launch_kernel(pdl, state_passing_scalar_kernel<uint16_t>, dim3(blocks), dim3(256), 0, st, static_cast<const uint16_t*>(S), cs2,
                         init, static_cast<uint16_t*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
     else
-      return launch_pdl(state_passing_scalar_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
+      return launch_kernel(pdl, state_passing_scalar_kernel<float>, dim3(blocks), dim3(256), 0, st, static_cast<const float*>(S), cs2,
                         init, static_cast<float*>(hprev), final_state, p.H, PN, p.nc, p.Q, total);
   }
   return cudaGetLastError();
