@@ -260,7 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_B,
                          const __grid_constant__ CUtensorMap tm_C,
                          const __grid_constant__ CUtensorMap tm_h,  // hprev, or Z when WIDE
-                         const __grid_constant__ CUtensorMap tm_y, const ScParams prm) {
+                         const __grid_constant__ CUtensorMap tm_y,
+                         const __grid_constant__ CUtensorMap tm_x2,  // x in 256-row boxes (Q = 256)
+                         const ScParams prm) {
   using SM = ScSmem<NB>;
   extern __shared__ uint8_t smem_raw[];
   // align by pointer arithmetic on the __shared__ array so accesses stay shared-space
@@ -282,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_C);
     prefetch_tmap(&tm_h);
     prefetch_tmap(&tm_y);
+    prefetch_tmap(&tm_x2);
     const uint32_t counts[SM::kNumBars] = {
         1, 1, kMaskWarps, 1,                                  // cb_full cb_done cb_empty seg_free
         1, 1, WIDE ? kEpiWarps : 1, WIDE ? kEpiWarps : 1,     // hp_full[2] hp_empty[2]
@@ -354,14 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
         const uint32_t xb = bar(kXsFull0 + s);
         mbar_arrive_expect_tx(xb, jrows * 128 + 2 * jrows * 4);
-        for (int jb = 0; jb < jrows / 128; ++jb)
-          tma_load_3d(xs + SM::kXsX + jb * kBox128, &tm_x, xb, hh * 64, sg.c * Q + jb * 128, sg.b);
+        // a 256-row head's x as one box: a TMA operation costs the SM about the same for 128 or
+        // 256 rows, and the producer issues several per head
+        if (jrows == 256)
+          tma_load_3d(xs + SM::kXsX, &tm_x2, xb, hh * 64, sg.c * Q, sg.b);
+        else
+          tma_load_3d(xs + SM::kXsX, &tm_x, xb, hh * 64, sg.c * Q, sg.b);
       };
       // L2 prefetch of head hh's inputs (no shared memory, no barrier); hprev / Z, cs2 and dt come
       // from the previous kernels, so this runs only after grid_dep_wait
       auto prefetch_head = [&](const Segment& sg, int hh) {
         const int i0 = sg.mt * 128, jrows = i0 + 128;
-        for (int jb = 0; jb < jrows / 128; ++jb) tma_prefetch_3d(&tm_x, hh * 64, sg.c * Q + jb * 128, sg.b);
+        if (jrows == 256)
+          tma_prefetch_3d(&tm_x2, hh * 64, sg.c * Q, sg.b);
+        else
+          tma_prefetch_3d(&tm_x, hh * 64, sg.c * Q, sg.b);
         if (WIDE)
           tma_prefetch_3d(&tm_h, hh * 64, sg.c * Q + i0, sg.b);
         else
@@ -751,7 +761,7 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, st, maps[0], maps[1], maps[2], maps[3],
-                    maps[4], prm);
+                    maps[4], maps[5], prm);
 }
 
 }  // namespace
@@ -774,7 +784,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
     const cudaError_t e = launch_chunk_readout_tc(p, C, cs2, hprev, zbuf, status, st, why);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap maps[5];  // x, B, C, hprev or Z, y
+  CUtensorMap maps[6];  // x, B, C, hprev or Z, y, x in 256-row boxes
   const uint64_t xdims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t xstr[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
   const uint64_t bdims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
@@ -798,6 +808,14 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
       !encode_tmap(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, xdims, xstr, box3,
                    CU_TENSOR_MAP_SWIZZLE_128B, why))
     return cudaErrorInvalidValue;
+  if (p.Q == 256) {
+    const uint32_t box256[3] = {64, 256, 1};
+    if (!encode_tmap(&maps[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xdims, xstr, box256,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  } else {
+    maps[5] = maps[0];  // never used: every head is 128 rows wide
+  }
   ScParams prm;
   prm.L = static_cast<int32_t>(p.L);
   prm.H = static_cast<int32_t>(p.H);
