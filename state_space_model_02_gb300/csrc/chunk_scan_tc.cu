@@ -100,9 +100,8 @@ struct ScSmem {
   static constexpr uint32_t kHpBytes = NB * kBox64;          // hprev slot: 64 p x N (bf16)
   static constexpr uint32_t kHp0 = kP + kPBytes;
   static constexpr uint32_t kXsX = 0;                        // x slot: 32 KB x (up to 256 tokens x 64 p)
-  static constexpr uint32_t kXsCs = 32768;                   //         1 KB cs2 row of the chunk
-  static constexpr uint32_t kXsDt = kXsCs + 1024;            //         1 KB dt row of the chunk
-  static constexpr uint32_t kXsBytes = kXsDt + 1024;
+  static constexpr uint32_t kXsCs = 32768;                   //         cs2 row, then dt row (Q floats each)
+  static constexpr uint32_t kXsBytes = kXsCs + 2048;
   static constexpr uint32_t kXs0 = kHp0 + 2 * kHpBytes;
   static constexpr uint32_t kY = kXs0 + 2 * kXsBytes;        // 16 KB: y staging (128 rows x 128 B)
   static constexpr uint32_t kColf = kY + kBox128;            // 2 x 1 KB: per-head column factors
@@ -262,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_h,  // hprev, or Z when WIDE
                          const __grid_constant__ CUtensorMap tm_y,
                          const __grid_constant__ CUtensorMap tm_x2,  // x in 256-row boxes (Q = 256)
+                         const __grid_constant__ CUtensorMap tm_cd,  // (cs2 row, dt row) pairs
                          const ScParams prm) {
   using SM = ScSmem<NB>;
   extern __shared__ uint8_t smem_raw[];
@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_h);
     prefetch_tmap(&tm_y);
     prefetch_tmap(&tm_x2);
+    prefetch_tmap(&tm_cd);
     const uint32_t counts[SM::kNumBars] = {
         1, 1, kMaskWarps, 1,                                  // cb_full cb_done cb_empty seg_free
         1, 1, WIDE ? kEpiWarps : 1, WIDE ? kEpiWarps : 1,     // hp_full[2] hp_empty[2]
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jrows = sg.mt * 128 + 128;
         const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
         const uint32_t xb = bar(kXsFull0 + s);
-        mbar_arrive_expect_tx(xb, jrows * 128 + 2 * jrows * 4);
+        mbar_arrive_expect_tx(xb, jrows * 128 + 2 * Q * 4);
         // a 256-row head's x as one box: a TMA operation costs the SM about the same for 128 or
         // 256 rows, and the producer issues several per head
         if (jrows == 256)
@@ -376,9 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_prefetch_3d(&tm_h, hh * 64, sg.c * Q + i0, sg.b);
         else
           tma_prefetch_3d(&tm_h, 0, ((sg.b * prm.nc + sg.c) * H + hh) * 64, 0);
-        const int64_t crow = ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q;
-        bulk_prefetch_l2(prm.cs2 + crow, jrows * 4);
-        bulk_prefetch_l2(prm.dtT + crow, jrows * 4);
+        tma_prefetch_3d(&tm_cd, 0, int32_t((int64_t(sg.b) * H + hh) * prm.nc + sg.c), 0);
       };
       // C, B and x are inputs of the step, not written by the kernels before this one (and every
       // kernel before the previous one has completed): the first segment's C and B and the first
@@ -428,9 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t xs = sb + SM::kXs0 + s * SM::kXsBytes;
             const uint32_t xb = bar(kXsFull0 + s);
             if (gi >= uint32_t(pre_x)) load_x(sg, hh, s);
-            const int64_t crow = ((int64_t(sg.b) * H + hh) * prm.nc + sg.c) * Q;
-            bulk_load(xs + SM::kXsCs, prm.cs2 + crow, jrows * 4, xb);
-            bulk_load(xs + SM::kXsDt, prm.dtT + crow, jrows * 4, xb);
+            // the head's cs2 and dt rows as one box of the (Q, row, array) view
+            tma_load_3d(xs + SM::kXsCs, &tm_cd, xb, 0, int32_t((int64_t(sg.b) * H + hh) * prm.nc + sg.c), 0);
             pend_xs[s] = true;
             ph_xs[s] = use & 1;
           }
@@ -603,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = gi & 1;
         const uint8_t* xsp = smem + SM::kXs0 + s * SM::kXsBytes;
         const float* cs = reinterpret_cast<const float*>(xsp + SM::kXsCs);
-        const float* dtv = reinterpret_cast<const float*>(xsp + SM::kXsDt);
+        const float* dtv = cs + Q;  // the dt row follows the cs2 row
         float* colf = reinterpret_cast<float*>(smem + SM::kColf + (gi & 1) * 1024);
         const bool have = mbar_wait(bar(kXsFull0 + s), (gi >> 1) & 1, ctl);
         if (have && mt_thread < jrows)
@@ -761,7 +759,7 @@ cudaError_t launch_nb(const CUtensorMap* maps, const ScParams& prm, int grid, cu
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), SM::kAlloc, st, maps[0], maps[1], maps[2], maps[3],
-                    maps[4], maps[5], prm);
+                    maps[4], maps[5], maps[6], prm);
 }
 
 }  // namespace
@@ -784,7 +782,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
     const cudaError_t e = launch_chunk_readout_tc(p, C, cs2, hprev, zbuf, status, st, why);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap maps[6];  // x, B, C, hprev or Z, y, x in 256-row boxes
+  CUtensorMap maps[7];  // x, B, C, hprev or Z, y, x in 256-row boxes, (cs2, dt) row pairs
   const uint64_t xdims[3] = {uint64_t(p.H * p.P), uint64_t(p.L), uint64_t(p.b)};
   const uint64_t xstr[2] = {uint64_t(p.H * p.P * 2), uint64_t(p.L * p.H * p.P * 2)};
   const uint64_t bdims[3] = {uint64_t(p.G * p.N), uint64_t(p.L), uint64_t(p.b)};
@@ -815,6 +813,22 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const void* x, const void* B,
       return cudaErrorInvalidValue;
   } else {
     maps[5] = maps[0];  // never used: every head is 128 rows wide
+  }
+  {
+    // cs2 and dtT (b, H, nc, Q) float32 as one (Q, b H nc, 2) view: the dt array sits at a fixed
+    // byte distance after the cs2 array, so one box {Q, 1, 2} brings a head's two rows
+    const int64_t gap = reinterpret_cast<const char*>(dtT) - reinterpret_cast<const char*>(cs2);
+    const int64_t rows = p.b * p.H * p.nc;
+    if (gap < rows * p.Q * 4 || gap % 16 != 0) {
+      if (why) *why = "chunk_scan needs the dt array after the cs2 array (the workspace layout)";
+      return cudaErrorInvalidValue;
+    }
+    const uint64_t dims[3] = {uint64_t(p.Q), uint64_t(rows), 2};
+    const uint64_t strides[2] = {uint64_t(p.Q * 4), uint64_t(gap)};
+    const uint32_t box[3] = {uint32_t(p.Q), 1, 2};
+    if (!encode_tmap(&maps[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, cs2, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, why))
+      return cudaErrorInvalidValue;
   }
   ScParams prm;
   prm.L = static_cast<int32_t>(p.L);
