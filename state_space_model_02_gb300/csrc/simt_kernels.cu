@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256, 3) chunk_state_simt_kernel(
 // factor above 1, bounded by 2^{cs2_j0 - cs2_j1}.  A block that holds such rows and decays by
 // more than kMaxFactorSpan (log2 units) takes each weight as one exp2 of its own instead.
 template <typename IO, typename HT>
-__global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
+__global__ void __launch_bounds__(256, 2) chunk_scan_simt_kernel(
     const IO* __restrict__ x, const IO* __restrict__ Bm, const IO* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ cs2, const float* __restrict__ dtT,
     const HT* __restrict__ hprev, IO* __restrict__ y, int64_t L, int64_t H, int64_t P, int64_t N,
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
   __shared__ __align__(16) float As[KT][GS];
   __shared__ __align__(16) float Bs[KT][GS];
   __shared__ float cs_i[TM], e_i[TM];
+  __shared__ float csq[256], dtq[256];  // the current head's cs2 and dt rows of the chunk (Q <= 256)
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int64_t i0 = int64_t(blockIdx.y) * TM;
   const int64_t bc = blockIdx.x, b = bc / nc, c = bc % nc;
@@ -137,109 +138,182 @@ __global__ void __launch_bounds__(256, 3) chunk_scan_simt_kernel(
   const int64_t h_begin = g * hpg + part * per, h_end = min(g * hpg + hpg, h_begin + per);
   const int64_t jmax = i0 + TM < Q ? i0 + TM : Q;  // columns j < jmax can be causal for these rows
   auto row_ok = [&](int64_t i_chunk) { return i_chunk < Q && c * Q + i_chunk < L; };
+  // Every operand tile is 16 x 64 values, four per thread.  The loops below run over flat
+  // sequences of tiles, and the next tile's global loads go into registers before the current
+  // tile's products, so their latency overlaps the products.  For the C-major fills
+  // (k = state column, consecutive threads read consecutive columns) element e = tid + 256 m is
+  // (row e / KT, k = e % KT); for the x fill it is (k = e / TM, column e % TM).
+  constexpr int kPer = KT * TM / 256;
+  float ra[kPer], rb[kPer];
+  auto load_c_rows = [&](int64_t n0) {  // ra: C rows of the tile, transposed on the store
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int e = tid + 256 * m, r = e / KT, k = e % KT;
+      const int64_t n = n0 + k, ti = i0 + r;
+      ra[m] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
+    }
+  };
+  auto store_rows = [&]() {  // ra -> As, rb -> Bs, both transposed (k-major)
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int e = tid + 256 * m, r = e / KT, k = e % KT;
+      As[k][r] = ra[m];
+      Bs[k][r] = rb[m];
+    }
+  };
 
-  // Phase 1: the causal C . B^T of the tile's rows, head-independent
-  for (int64_t j0 = 0; j0 < jmax; j0 += TM) {
+  // Phase 1: the causal C . B^T of the tile's rows, head-independent; (j0, n0) tiles in order
+  const int64_t nn = (N + KT - 1) / KT, n_cb = ((jmax + TM - 1) / TM) * nn;
+  auto load_cb = [&](int64_t t) {
+    const int64_t j0 = (t / nn) * TM, n0 = (t % nn) * KT;
+    load_c_rows(n0);
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int e = tid + 256 * m, r = e / KT, k = e % KT;
+      const int64_t n = n0 + k, tj = j0 + r;
+      rb[m] = (row_ok(tj) && n < N) ? ld_io(Bm, ((b * L + c * Q + tj) * G + g) * N + n) : 0.f;
+    }
+  };
+  {
     float acc[4][4] = {};
-    for (int64_t n0 = 0; n0 < N; n0 += KT) {
-      for (int e = tid; e < KT * TM; e += 256) {
-        const int r = e / KT, k = e % KT;  // consecutive threads read consecutive n
-        const int64_t n = n0 + k;
-        const int64_t ti = i0 + r, tj = j0 + r;
-        As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
-        Bs[k][r] = (row_ok(tj) && n < N) ? ld_io(Bm, ((b * L + c * Q + tj) * G + g) * N + n) : 0.f;
-      }
+    load_cb(0);
+    for (int64_t t = 0; t < n_cb; ++t) {
+      store_rows();
       __syncthreads();
+      if (t + 1 < n_cb) load_cb(t + 1);
 #pragma unroll
       for (int k = 0; k < KT; ++k)
         mma4x4(acc, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
       __syncthreads();
-    }
+      if (t % nn == nn - 1) {
+        const int64_t j0 = (t / nn) * TM;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int64_t j = j0 + 4 * tx + cc;
-      if (j >= jmax) continue;
-      float v[4];
+        for (int cc = 0; cc < 4; ++cc) {
+          const int64_t j = j0 + 4 * tx + cc;
+          if (j < jmax) {
+            float v[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) v[r] = (j <= i0 + 4 * ty + r) ? acc[r][cc] : 0.f;
-      *reinterpret_cast<float4*>(&CBs[j * GS + 4 * ty]) = make_float4(v[0], v[1], v[2], v[3]);
+            for (int r = 0; r < 4; ++r) v[r] = (j <= i0 + 4 * ty + r) ? acc[r][cc] : 0.f;
+            *reinterpret_cast<float4*>(&CBs[j * GS + 4 * ty]) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[r][cc] = 0.f;
+        }
+      }
     }
   }
 
-  for (int64_t h = h_begin; h < h_end; ++h) {
-    const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
-    const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
-    __syncthreads();  // CBs complete / the previous head done with cs_i, As, Bs
-    if (tid < TM) {
-      const bool in = i0 + tid < Q;
-      cs_i[tid] = in ? csr[i0 + tid] : 0.f;
-      e_i[tid] = in ? ex2(csr[i0 + tid]) : 0.f;
-    }
-    __syncthreads();
-    const float Dh = D ? D[h] : 0.f;
-    const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
-    for (int64_t p0 = 0; p0 < P; p0 += TM) {
-      float acc1[4][4] = {}, acc2[4][4] = {};
-      for (int64_t j0 = 0; j0 < jmax; j0 += KT) {
-        const float cj1 = csr[j0 + KT - 1];
-        // uniform over the CTA: a block left of every row of the tile (j0 < i0) always factors
-        const bool factored = j0 < i0 || fabsf(csr[j0] - cj1) <= kMaxFactorSpan;
-        for (int e = tid; e < KT * TM; e += 256) {
-          const int k = e / TM, col = e % TM;
-          const int64_t tj = j0 + k;
-          float v = 0.f;
-          if (row_ok(tj) && p0 + col < P)
-            v = ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) *
-                (factored ? ex2(cj1 - csr[tj]) * dtr[tj] : dtr[tj]);
-          Bs[k][col] = v;
-        }
-        __syncthreads();
-        if (factored) {
-          float part_acc[4][4] = {};
+  // Phase 2: per head and 64-column p tile, n1 tiles of Y1 = (L o CB) x (x rows j0 .. j0 + KT)
+  // then n2 tiles of Y2 = C hprev^T (state columns n0 .. n0 + KT), one flat sequence over the
+  // CTA's heads
+  const int64_t np = (P + TM - 1) / TM, n1 = (jmax + KT - 1) / KT, n2 = nn;
+  const int64_t per_tile = n1 + n2, per_head = np * per_tile, n_all = (h_end - h_begin) * per_head;
+  auto load_tile = [&](int64_t t) {
+    const int64_t h = h_begin + t / per_head, rem = t % per_head;
+    const int64_t p0 = (rem / per_tile) * TM, q = rem % per_tile;
+    if (q < n1) {
+      const int64_t j0 = q * KT;
 #pragma unroll
-          for (int k = 0; k < KT; ++k)
-            mma4x4(part_acc, *reinterpret_cast<const float4*>(&CBs[(j0 + k) * GS + 4 * ty]),
-                   *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+      for (int m = 0; m < kPer; ++m) {
+        const int e = tid + 256 * m, k = e / TM, col = e % TM;
+        const int64_t tj = j0 + k;
+        ra[m] = (row_ok(tj) && p0 + col < P) ? ld_io(x, ((b * L + c * Q + tj) * H + h) * P + p0 + col) : 0.f;
+      }
+    } else {
+      const int64_t n0 = (q - n1) * KT;
+      load_c_rows(n0);
+      const HT* hp = hprev + (((b * nc + c) * H + h) * P) * N;
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int e = tid + 256 * m, r = e / KT, k = e % KT;
+        const int64_t n = n0 + k;
+        rb[m] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
+      }
+    }
+  };
+  float acc1[4][4], acc2[4][4];
+  if (n_all > 0) load_tile(0);
+  for (int64_t t = 0; t < n_all; ++t) {
+    const int64_t h = h_begin + t / per_head, rem = t % per_head;
+    const int64_t p0 = (rem / per_tile) * TM, q = rem % per_tile;
+    if (rem == 0) {
+      // a new head: its cs2 / dt rows (the previous head's epilogue has read e_i)
+      const float* csr = cs2 + ((b * H + h) * nc + c) * Q;
+      const float* dtr = dtT + ((b * H + h) * nc + c) * Q;
+      __syncthreads();
+      if (tid < TM) {
+        const bool in = i0 + tid < Q;
+        cs_i[tid] = in ? csr[i0 + tid] : 0.f;
+        e_i[tid] = in ? ex2(csr[i0 + tid]) : 0.f;
+      }
+      for (int64_t j = tid; j < Q; j += 256) {
+        csq[j] = csr[j];
+        dtq[j] = dtr[j];
+      }
+      __syncthreads();
+    }
+    if (q == 0) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = acc2[r][cc] = 0.f;
+    }
+    if (q < n1) {
+      const int64_t j0 = q * KT;
+      const float cj1 = csq[j0 + KT - 1];
+      // uniform over the CTA: a block left of every row of the tile (j0 < i0) always factors
+      const bool factored = j0 < i0 || fabsf(csq[j0] - cj1) <= kMaxFactorSpan;
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int e = tid + 256 * m, k = e / TM, col = e % TM;
+        const int tj = int(j0) + k;
+        Bs[k][col] = ra[m] * (factored ? ex2(cj1 - csq[tj]) * dtq[tj] : dtq[tj]);
+      }
+      __syncthreads();
+      if (t + 1 < n_all) load_tile(t + 1);
+      if (factored) {
+        float part_acc[4][4] = {};
+#pragma unroll
+        for (int k = 0; k < KT; ++k)
+          mma4x4(part_acc, *reinterpret_cast<const float4*>(&CBs[(j0 + k) * GS + 4 * ty]),
+                 *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int il = 4 * ty + r;
+          const float rf = (j0 <= i0 + il) ? ex2(cs_i[il] - cj1) : 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(rf, part_acc[r][cc], acc1[r][cc]);
+        }
+      } else {
+        // every weight 2^{cs2_i - cs2_j} (j <= i) on its own; CBs is already zero for j > i
+#pragma unroll 4
+        for (int k = 0; k < KT; ++k) {
+          const int64_t j = j0 + k;
+          const float cjk = csq[j];
+          const float4 cb = *reinterpret_cast<const float4*>(&CBs[j * GS + 4 * ty]);
+          const float4 xv = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
+          const float cbv[4] = {cb.x, cb.y, cb.z, cb.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int il = 4 * ty + r;
-            const float rf = (j0 <= i0 + il) ? ex2(cs_i[il] - cj1) : 0.f;
+            const float a = j <= i0 + il ? cbv[r] * ex2(cs_i[il] - cjk) : 0.f;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(rf, part_acc[r][cc], acc1[r][cc]);
-          }
-        } else {
-          // every weight 2^{cs2_i - cs2_j} (j <= i) on its own; CBs is already zero for j > i
-#pragma unroll 4
-          for (int k = 0; k < KT; ++k) {
-            const int64_t j = j0 + k;
-            const float cjk = csr[j];
-            const float4 cb = *reinterpret_cast<const float4*>(&CBs[j * GS + 4 * ty]);
-            const float4 xv = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
-            const float cbv[4] = {cb.x, cb.y, cb.z, cb.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int il = 4 * ty + r;
-              const float a = j <= i0 + il ? cbv[r] * ex2(cs_i[il] - cjk) : 0.f;
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(a, xw[cc], acc1[r][cc]);
-            }
+            for (int cc = 0; cc < 4; ++cc) acc1[r][cc] = fmaf(a, xw[cc], acc1[r][cc]);
           }
         }
-        __syncthreads();
       }
-      for (int64_t n0 = 0; n0 < N; n0 += KT) {
-        for (int e = tid; e < KT * TM; e += 256) {
-          const int r = e / KT, k = e % KT;
-          const int64_t n = n0 + k, ti = i0 + r;
-          As[k][r] = (row_ok(ti) && n < N) ? ld_io(Cm, ((b * L + c * Q + ti) * G + g) * N + n) : 0.f;
-          Bs[k][r] = (p0 + r < P && n < N) ? ld_io(hp, (p0 + r) * N + n) : 0.f;
-        }
-        __syncthreads();
+      __syncthreads();
+    } else {
+      store_rows();
+      __syncthreads();
+      if (t + 1 < n_all) load_tile(t + 1);
 #pragma unroll
-        for (int k = 0; k < KT; ++k)
-          mma4x4(acc2, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
-        __syncthreads();
-      }
+      for (int k = 0; k < KT; ++k)
+        mma4x4(acc2, *reinterpret_cast<const float4*>(&As[k][4 * ty]), *reinterpret_cast<const float4*>(&Bs[k][4 * tx]));
+      __syncthreads();
+    }
+    if (q == per_tile - 1) {
+      const float Dh = D ? D[h] : 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int il = 4 * ty + r;
