@@ -27,7 +27,8 @@
 //   warp 0      TMA producer: C and B per segment; per head hprev (2-slot ring, freed once Y2
 //               is done; one box) and x, cs2, dt (2-slot ring, freed once Y1 and the mask are
 //               done).  A TMA box costs the SM about the same for 64 or 128 rows, so operands
-//               come in few, large boxes and nothing is prefetched separately;
+//               come in few, large boxes; the inputs of the head kPrefetchAhead places ahead
+//               are prefetched into L2;
 //   warp 1      tcgen05.mma issuer; owns the TMEM allocation.  It touches no shared memory
 //               between MMAs (such an access waits for the MMAs already queued): warp 22
 //               waits on its mbarriers and hands over through a named barrier

@@ -111,6 +111,7 @@ EDGE = [
     dict(batch=2, seqlen=600, nheads=3, headdim=64, dstate=384, chunk=128),   # wide state, Q = 128
     dict(batch=1, seqlen=520, nheads=4, headdim=64, dstate=256, ngroups=2, chunk=256),  # wide x groups
     dict(batch=1, seqlen=500, nheads=5, headdim=64, dstate=192, chunk=128),   # wide, 3 K steps
+    dict(batch=1, seqlen=333, nheads=5, headdim=96, dstate=80, chunk=128),    # CUDA cores: ragged p tile
 ]
 
 
