@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       grid_dep_wait();
       for (SegWalk w = walk0; w.more(); ++si) {
         const Segment sg = w.seg(prm);
-        const int i0 = sg.mt * 128, jrows = i0 + 128;
+        const int i0 = sg.mt * 128;
         // C and B of the new segment overwrite regions the previous segment's MMAs read
         if (si >= 1) (void)mbar_wait(bar(kSegFree), (si - 1) & 1, ctl);
         if (WIDE) {
