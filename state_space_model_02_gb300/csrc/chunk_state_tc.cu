@@ -127,9 +127,10 @@ __device__ __forceinline__ bool local_item(uint32_t j, const CsParams& prm, Item
   return true;
 }
 
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float w) {
-  return pack_bf16x2(bf16lo_to_f32(v) * w, bf16hi_to_f32(v) * w);
-}
+// x~ = w x on a packed bf16 pair: w is rounded to bf16 too (one more rounding of the same size
+// as the product's), so the pair takes one bf16x2 multiply instead of an unpack, two float
+// multiplies and a repack -- the scaling pass sits between every k-block's load and its MMAs.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, uint32_t w2) { return mul_bf16x2(v, w2); }
 
 // FUSED: fwd_pass_state in one kernel -- instead of storing S, the epilogue carries each chain's
 // float32 state in tensor memory (h <- 2^{cs2_last} h + S_c, chunk by chunk), stores the state
@@ -300,12 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = ts + 128 * j;
             const int k = q >> 9, r = (q >> 3) & 63;
             const float w = wsm[k * 256 + kb * 64 + r];
+            const uint32_t w2 = pack_bf16x2(w, w);
             uint4* pch = reinterpret_cast<uint4*>(xs + q * 16);
             uint4 v = *pch;
-            v.x = scale_bf16x2(v.x, w);
-            v.y = scale_bf16x2(v.y, w);
-            v.z = scale_bf16x2(v.z, w);
-            v.w = scale_bf16x2(v.w, w);
+            v.x = scale_bf16x2(v.x, w2);
+            v.y = scale_bf16x2(v.y, w2);
+            v.z = scale_bf16x2(v.z, w2);
+            v.w = scale_bf16x2(v.w, w2);
             *pch = v;
           }
           fence_proxy_async_smem();
@@ -589,12 +591,13 @@ __global__ void __launch_bounds__(kItemThreads, 1)
         const int q = tid + kItemThreads * i;
         const int k = q >> 9, r = (q >> 3) & 63;
         const float w = wsm[k * 256 + kb * 64 + r];
+        const uint32_t w2 = pack_bf16x2(w, w);
         uint4* p = reinterpret_cast<uint4*>(xs + q * 16);
         uint4 v = *p;
-        v.x = scale_bf16x2(v.x, w);
-        v.y = scale_bf16x2(v.y, w);
-        v.z = scale_bf16x2(v.z, w);
-        v.w = scale_bf16x2(v.w, w);
+        v.x = scale_bf16x2(v.x, w2);
+        v.y = scale_bf16x2(v.y, w2);
+        v.z = scale_bf16x2(v.z, w2);
+        v.w = scale_bf16x2(v.w, w2);
         *p = v;
       }
       fence_proxy_async_smem();
