@@ -17,9 +17,8 @@
 // against), copied through shared memory in the last chunk.
 //
 // Two kernels.  When dt's rows are 16-byte aligned (H a multiple of 4) and there are at least four
-// tiles per SM, persistent CTAs walk the tiles strided by the grid: TMA copies each (token, head)
-// tile of dt into one of four shared-memory stages, three tiles ahead of the one being scanned;
-// the lanes write their cs2 and dt runs as
+// tiles per SM, persistent CTAs walk the tiles strided by the grid: TMA copies each (token, head) tile of dt into one of two shared-
+// memory stages while the previous tile is scanned; the lanes write their cs2 and dt runs as
 // 16-byte vectors into head-major staging tiles (128-byte rows of 32 tokens, 16-byte chunks
 // XOR-swizzled by head so that 8 lanes of different heads hit 8 different bank groups), and TMA
 // stores send the staged rows out, so every global access is a whole tile (one load box and one
@@ -168,21 +167,18 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(const float* __restri
   if (head_ok) store_run<R>(cs2 + row, v);
 }
 
-constexpr int kTmaStages = 4;
+constexpr int kTmaStages = 2;
 
-// Shared memory of the TMA kernel: kTmaStages dt stages ((Q tokens x HT heads) float32,
-// token-major as dt lays it out) and one output slot, a cs2 tile and a dt tile in the swizzled
-// head-major layout the TMA stores read: Q/32 boxes of HT rows x 128 bytes (32 tokens of one
-// head).  Four input stages with one output slot measured faster than two of each (a stage's
-// next tile is requested as soon as the scan has read it; the output slot's previous stores
-// have read it by the time the scan is done).
+// Shared memory of the TMA kernel: two dt stages ((Q tokens x HT heads) float32, token-major as
+// dt lays it out) and two output slots, each a cs2 tile and a dt tile in the swizzled head-major
+// layout the TMA stores read: Q/32 boxes of HT rows x 128 bytes (32 tokens of one head).
 template <int Q, int HT>
 struct TmaSmem {
   static constexpr uint32_t kTile = Q * HT * 4;
   static constexpr uint32_t kBox = HT * 128;  // one store box: 32 tokens of every head
   static constexpr uint32_t kIn = 0;
-  static constexpr uint32_t kOut = kTmaStages * kTile;  // the output slot: cs2 tile, then dt tile
-  static constexpr uint32_t kAlloc = kOut + 2 * kTile + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t kOut = kTmaStages * kTile;  // slot o: cs2 at kOut + 2 o kTile, dt after
+  static constexpr uint32_t kAlloc = kOut + 4 * kTile + 1024;  // + slack for 1024-byte alignment
   static_assert(kBox % 1024 == 0, "store boxes must stay 1024-byte aligned for the 128-byte swizzle");
 };
 
@@ -194,9 +190,9 @@ __device__ __forceinline__ uint32_t out_offset(int hl, int t) {
 }
 
 // Persistent CTAs; tile t = (c, b, head tile z), c fastest; CTA k takes t = k, k + grid, ...
-// Thread 0 keeps the next tiles' copies in flight in the other dt stages, refilling a stage once
-// every thread has read it, and issues the stores of a tile's staged outputs; the staging is
-// rewritten by the next tile, after thread 0 has seen the stores finish reading it.
+// Thread 0 keeps the next tile's copy in flight in the other dt stage, refilling a stage once
+// every thread has read it, and issues the stores of a tile's staged outputs; a slot's staging is
+// rewritten two tiles later, after thread 0 has seen that slot's stores finish reading it.
 // Waits are bounded: on expiry the status word records SSD_ERR_TIMEOUT and the CTA runs its loop
 // to the end without copying or storing anything more.
 template <int Q, int HT>
@@ -251,7 +247,7 @@ __global__ void __launch_bounds__(256) chunk_cumsum_tma_kernel(const __grid_cons
   }
   int k = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++k) {
-    const int s = k % kTmaStages;
+    const int s = k % kTmaStages, o = k & 1;
     const uint32_t parity = uint32_t(k / kTmaStages) & 1u;
     const int64_t c = t % nc, rest = t / nc, b = rest % nb, z = rest / nb;
     const int64_t h = z * HT + hl;
@@ -260,27 +256,20 @@ __global__ void __launch_bounds__(256) chunk_cumsum_tma_kernel(const __grid_cons
     // rows past L and heads past H arrive as zeros (the copy's out-of-bounds fill)
     const float* tile = reinterpret_cast<const float*>(smem + SM::kIn + s * SM::kTile);
     const float a = h < H ? __ldg(A + h) : 0.f;
-    float v[R], raw[R];
+    float v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      raw[r] = ok ? tile[(t0 + r) * HT + hl] : 0.f;
-      v[r] = raw[r] * a;
-    }
+    for (int r = 0; r < R; ++r) v[r] = ok ? tile[(t0 + r) * HT + hl] * a : 0.f;
+    // slot o's stores of two tiles ago must have read their staging before it is rewritten;
+    // the scan's barrier publishes that to every thread
+    if (threadIdx.x == 0) bulk_wait_read<1>();
     scan_core<Q, HT>(v, c, L, t0, warp_total[k & 1], last_cs);
-    // the one staging slot: the previous tile's stores must have read it (published by the
-    // barrier); past the scan's barrier every thread has also read stage s, so its next tile
-    // can be requested now, a whole staging and store ahead of where the tile loop ends
-    if (threadIdx.x == 0) bulk_wait_read<0>();
-    __syncthreads();
-    if (threadIdx.x == 0 && !*abort_flag && t + int64_t(kTmaStages) * gridDim.x < ntiles)
-      issue(t + int64_t(kTmaStages) * gridDim.x, s, parity ^ 1u);
     if (ok) {
-      uint8_t* out_cs = smem + SM::kOut;
+      uint8_t* out_cs = smem + SM::kOut + 2 * o * SM::kTile;
       uint8_t* out_dt = out_cs + SM::kTile;
       const int64_t left = L - (c * Q + t0);
       float d[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) d[r] = unit_scale ? (r < left ? 1.f : 0.f) : raw[r];
+      for (int r = 0; r < R; ++r) d[r] = unit_scale ? (r < left ? 1.f : 0.f) : tile[(t0 + r) * HT + hl];
       if constexpr (R % 4 == 0) {
 #pragma unroll
         for (int r = 0; r < R; r += 4) {
@@ -298,7 +287,7 @@ __global__ void __launch_bounds__(256) chunk_cumsum_tma_kernel(const __grid_cons
     fence_proxy_async_smem();
     __syncthreads();  // staging written, stage s read by every thread
     if (threadIdx.x == 0 && !*abort_flag) {
-      const uint32_t out_cs = sb + SM::kOut, out_dt = out_cs + SM::kTile;
+      const uint32_t out_cs = sb + SM::kOut + 2 * o * SM::kTile, out_dt = out_cs + SM::kTile;
       if (one_box) {  // the whole staged tile as one box of the 5-D view
         tma_store_5d(&tm_cs, out_cs, 0, int32_t(z * HT), 0, int32_t(c), int32_t(b));
         tma_store_5d(&tm_dtT, out_dt, 0, int32_t(z * HT), 0, int32_t(c), int32_t(b));
@@ -309,6 +298,7 @@ __global__ void __launch_bounds__(256) chunk_cumsum_tma_kernel(const __grid_cons
         }
       }
       bulk_commit();
+      if (t + int64_t(kTmaStages) * gridDim.x < ntiles) issue(t + int64_t(kTmaStages) * gridDim.x, s, parity ^ 1u);
     }
   }
   // every copy issued must have landed, and every store completed, before the CTA exits
