@@ -19,10 +19,13 @@
 //               two heads' cs2 / dt rows (bulk copies) into one of two weight windows;
 //   warp 1      tcgen05.mma issuer: per k-block 4 MMAs (M = 2 x P = 128, N = NT, K = 16) into
 //               one of two TMEM accumulators (the item's parity);
-//   warps 2-5   the decay weights w_t = 2^{cs2_last - cs2_t} dt_t of each item, then x~ = w x
+//   warps 2-9   the decay weights w_t = 2^{cs2_last - cs2_t} dt_t of each item, then x~ = w x
 //               in place in every stage (one weight per 128-byte row, so the swizzle does not
 //               matter);
-//   warps 6-9   epilogue: accumulator -> bf16 -> swizzled staging -> TMA store of S.
+//   warps 10-13 epilogue: accumulator -> bf16 -> swizzled staging -> TMA store of S.
+// The scaling of a k-block stands between its load and its MMAs, so eight warps share it (four
+// 16-byte chunks a thread): against four warps (eight chunks a thread) that took chunk_state
+// from 313 to 284 us at 256K tokens; sixteen warps measured 290 us.
 // Every wait is bounded; after an expiry the roles keep their loop counts but skip their work,
 // then drain their own copies and MMAs and release TMEM.
 // Requirements (checked by chunk_state_tc_ok): bf16 I/O, P = 64, Q in {128, 256},
@@ -33,9 +36,9 @@
 namespace ssd {
 namespace {
 
-constexpr int kWarps = 10;
+constexpr int kWarps = 14;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kScaleWarp0 = 2, kEpiWarp0 = 6;
+constexpr int kScaleWarp0 = 2, kEpiWarp0 = 10;
 constexpr uint32_t kBox = 8192;  // one TMA box: 64 rows x 128 bytes
 constexpr uint32_t kBarScale = 1, kBarEpi = 2;  // named barriers of the scale and epilogue groups
 
@@ -162,12 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_S);
     for (int i = 0; i < S; ++i) {
       mbar_init(bar(SM::kFull + i), 1);
-      mbar_init(bar(SM::kScaled + i), 4);
+      mbar_init(bar(SM::kScaled + i), 8);
       mbar_init(bar(SM::kEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SM::kWinFull + i), 1);
-      mbar_init(bar(SM::kWinEmpty + i), 4);
+      mbar_init(bar(SM::kWinEmpty + i), 8);
       mbar_init(bar(SM::kAccFull + i), 1);
       mbar_init(bar(SM::kAccEmpty + i), 4);
     }
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------- decay weights, x~ = w x in place
-    const int ts = threadIdx.x - 32 * kScaleWarp0;  // 0..127
+    const int ts = threadIdx.x - 32 * kScaleWarp0;  // 0..255
     uint32_t gk = 0, it_local = 0;
     for (;; ++it_local) {
       Item it;
@@ -282,23 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have = mbar_wait(bar(SM::kWinFull + ws), (it_local >> 1) & 1, ctl);
       const float* win = reinterpret_cast<const float*>(smem + SM::kWin + ws * SM::kWinBytes);
       float* wsm = reinterpret_cast<float*>(smem + SM::kW + ws * 2048);
-      for (int e = ts; e < 2 * Q; e += 128) {
+      for (int e = ts; e < 2 * Q; e += 256) {
         const int k = e / Q, t = e % Q;
         // w[k][t] = 2^(cs2_last - cs2_t) dt_t; zero for a missing second head
         wsm[k * 256 + t] = have && k < it.nh ? ex2(win[k * 256 + Q - 1] - win[k * 256 + t]) * win[512 + k * 256 + t] : 0.f;
       }
-      named_bar_sync(kBarScale, 128);
+      named_bar_sync(kBarScale, 256);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SM::kWinEmpty + ws));
       for (int kb = 0; kb < kblocks; ++kb, ++gk) {
         const int s = static_cast<int>(gk % S);
         const bool ok = mbar_wait(bar(SM::kFull + s), (gk / S) & 1, ctl) && !*abort_flag;
         if (ok) {
-          // 1024 16-byte chunks (two boxes x 64 rows x 8), 8 per thread
+          // 1024 16-byte chunks (two boxes x 64 rows x 8), 4 per thread
           uint8_t* xs = smem + s * SM::kStage;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int q = ts + 128 * j;
+          for (int j = 0; j < 4; ++j) {
+            const int q = ts + 256 * j;
             const int k = q >> 9, r = (q >> 3) & 63;
             const float w = wsm[k * 256 + kb * 64 + r];
             const uint32_t w2 = pack_bf16x2(w, w);
