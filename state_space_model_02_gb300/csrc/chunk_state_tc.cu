@@ -474,14 +474,16 @@ cudaError_t launch_nt(const CUtensorMap& tx, const CUtensorMap& tb, const CUtens
 
 // ---- one CTA per work item: the first design, kept for problems with few items per SM ----
 //
-// One CTA = (head pair, n-tile, chunk, batch), 128 threads, no warp specialisation: thread 0
+// One CTA = (head pair, n-tile, chunk, batch), 256 threads, no warp specialisation: thread 0
 // issues TMA loads (2-stage ring over 64-token k-blocks) and the MMAs; all threads scale the x
 // tile in shared memory by the decay weight, then drain the f32 accumulator from tensor memory
-// and stage it, rounded to bf16, for TMA stores of S.  Several CTAs share an SM, so their
+// (two warps per lane quarter, one column half each) and stage it, rounded to bf16, for TMA
+// stores of S.  256 threads instead of 128 halve each k-block's scaling pass: 16K-token sweeps
+// N = 64 / 128 / 256 29.7 -> 27.3, 37.5 -> 33.4, 53 -> 45 us.  Several CTAs share an SM, so their
 // load, MMA and store phases overlap one another; with a few items per SM that beats the
 // persistent kernel's single pipeline (130M layer 15.5 against 18.4 us), with many it loses
 // (2.7B layer 62 against 58 us, 256K tokens 366 against 316 us).
-constexpr int kItemThreads = 128;
+constexpr int kItemThreads = 256;
 
 template <int NT>
 struct ItemSmem {
@@ -587,10 +589,10 @@ __global__ void __launch_bounds__(kItemThreads, 1)
     const bool ok = mbar_wait(bar_full + 8 * s, ph, ctl);
     if (tid == 0 && ok) consumed = kb + 1;
     if (ok) {
-      // x~ = w * x in place: 1024 16-byte chunks (two boxes x 64 rows x 8), 8 per thread
+      // x~ = w * x in place: 1024 16-byte chunks (two boxes x 64 rows x 8), 4 per thread
       uint8_t* xs = smem + s * SM::kStage;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 1024 / kItemThreads; ++i) {
         const int q = tid + kItemThreads * i;
         const int k = q >> 9, r = (q >> 3) & 63;
         const float w = wsm[k * 256 + kb * 64 + r];
@@ -628,13 +630,15 @@ __global__ void __launch_bounds__(kItemThreads, 1)
   tc_fence_after();
 
   if (acc_ok) {
-    // S is stored in bf16: one 64 x 64 box (8 KB, 128-byte rows, swizzled) per (n block, head)
-    const int k = tid >> 6, r = tid & 63;
+    // S is stored in bf16: one 64 x 64 box (8 KB, 128-byte rows, swizzled) per (n block, head);
+    // warp w reads TMEM lane quarter w % 4 and the column half w / 4
+    const int quarter = warp & 3, half = warp >> 2;
+    const int rr = 32 * quarter + (tid & 31), k = rr >> 6, r = rr & 63;
 #pragma unroll 1
-    for (int q = 0; q < NT / 32; ++q) {
+    for (int q = half * (NT / 64); q < (half + 1) * (NT / 64); ++q) {
       uint32_t v[32];
       __syncwarp();
-      tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + q * 32, v);
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + q * 32, v);
       tmem_ld_wait();
       uint8_t* box = smem + ((q >> 1) * 2 + k) * kBox;
 #pragma unroll
